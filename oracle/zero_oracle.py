@@ -1,0 +1,434 @@
+"""CPU oracle for the ZeRO sharded-optimizer data-parallel hot path.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plain, single-threaded
+statement of what the hot path computes.  Only the test suite, the smoke check
+and the benchmark's CPU-baseline / reference legs may import it; the product
+library never calls it and shares no code, table or helper with it.
+
+Sources (web pages, cited by title and section):
+  [P1] "[REQUEST] Direct Correspondence between Gradient and Optimizer States
+       to Reduce Communication?" (DeepSpeed issue 4582), section "Problem":
+       partition gradients, reduce-scatter them to the owners of the optimizer
+       state, update the owners' parameters, all-gather the parameters.
+  [P2] "Why does not the stage 3 implementation use broadcast and
+       reduce-scatter?" (DeepSpeed issue 1173), answers: stage 3 gathers
+       parameters with all-gather; the gradient reduce-scatter is implemented
+       only over contiguous gradient buffers.
+  [P3] "Why DeepSpeed ZeRO paper says reduce-scatter (or all-gather) has data
+       movement of Psi elements?" (DeepSpeed discussion 6594): all-reduce =
+       reduce-scatter + all-gather, each moving Psi; the ring narration of the
+       reduce-scatter; the all-gather count.
+  [P4] "ZeRO Optimizer" (wiki page), sections "Memory Components",
+       "ZeRO Stages", "Implementation Strategy", "Theoretical Reductions".
+  [KB] Kingma and Ba, "Adam: A Method for Stochastic Optimization" (2015),
+       Algorithm 1 -- the pages name Adam's m and v but not its formula.
+
+Precision.  The workloads fix fp32 master weights, fp32 m and v, fp32 reduced
+gradients and bf16 gathered parameters, so the oracle does the method's
+arithmetic in fp32, one IEEE rounding per operation, in the order written
+below (numpy float32 ufuncs: no fused multiply-add, no reassociation).  The
+global gradient norm is accumulated in fp64.
+
+Readings where the pages leave a step open (each is listed with its reason in
+the design notes):
+  * flat buffer = the tensors concatenated in list order, padded only at the
+    tail to a multiple of N*align; rank r owns [r*S, (r+1)*S)   [P2], [P1]
+  * ring reduce-scatter: chunk k's partial sum starts at rank k+1 and travels
+    k+1 -> k+2 -> ... -> k, the owner adding its own chunk last, so each rank
+    sends and receives (N-1) chunks.  The narration in [P3] starts the chain
+    at the owner and sends the total back; ``narrated=True`` runs that
+    literal form (N sends per rank) to show where the two counts part.
+  * gradient scale 1/N after the sum, optional clip by global norm, then
+    standard Adam with bias correction [KB], fp32, in the order of
+    ``adam_update``.
+  * bf16 cast = round to nearest, ties to even, of the fp32 bit pattern.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+F32 = np.float32
+
+
+# ---------------------------------------------------------------------------
+# a1: plan -- flat contiguous buffer, N equal owner shards, tail padding
+# ---------------------------------------------------------------------------
+@dataclass
+class Group:
+    index: int
+    tensors: list          # tensor ids in list order
+    psi: int               # real elements in the group
+    psi_pad: int           # padded to a multiple of N*align
+    shard: int             # S = psi_pad / N
+    flat_off: int          # offset of the group in the group-major flat arrays
+    rank_off: int          # offset of the group inside each rank's shard buffer
+
+
+@dataclass
+class Plan:
+    numels: list
+    n_ranks: int
+    align: int
+    groups: list = field(default_factory=list)
+    tensor_group: list = field(default_factory=list)
+    tensor_group_off: list = field(default_factory=list)   # offset inside its group
+
+    @property
+    def psi(self) -> int:
+        return sum(g.psi for g in self.groups)
+
+    @property
+    def psi_pad(self) -> int:
+        return sum(g.psi_pad for g in self.groups)
+
+    @property
+    def shard_total(self) -> int:
+        return sum(g.shard for g in self.groups)
+
+    def tensor_flat_off(self, t: int) -> int:
+        return self.groups[self.tensor_group[t]].flat_off + self.tensor_group_off[t]
+
+    def owner_span(self, t: int):
+        """Ranks owning the first and the last element of tensor t; (-1, -1)
+        for an empty tensor."""
+        n = self.numels[t]
+        if n == 0:
+            return -1, -1
+        g = self.groups[self.tensor_group[t]]
+        off = self.tensor_group_off[t]
+        return off // g.shard, (off + n - 1) // g.shard
+
+    def shard_range(self, group: int, rank: int):
+        """(flat begin, length, real elements) of rank's shard of a group."""
+        g = self.groups[group]
+        begin = g.flat_off + rank * g.shard
+        valid = max(0, min(g.shard, g.psi - rank * g.shard))
+        return begin, g.shard, valid
+
+    def segments(self, rank: int):
+        """Pieces of tensors that rank owns: (tensor, tensor_off, flat_off, len),
+        in flat order."""
+        out = []
+        for g in self.groups:
+            lo_r, hi_r = rank * g.shard, (rank + 1) * g.shard
+            for t in g.tensors:
+                a = self.tensor_group_off[t]
+                b = a + self.numels[t]
+                lo, hi = max(a, lo_r), min(b, hi_r)
+                if hi > lo:
+                    out.append((t, lo - a, g.flat_off + lo, hi - lo))
+        return out
+
+    def memory(self, stage: int):
+        """Per-device memory of one rank.  Values follow [P4] "Theoretical
+        Reductions" (params P, grads P, optimizer states 2P; stage s shards
+        the first s of {optimizer states, gradients, parameters}); bytes use
+        bf16 params and grads and fp32 master + m + v (12 bytes per value).
+        stage 0 = plain data parallelism (4P values)."""
+        P, S = self.psi_pad, self.shard_total
+        values = {0: 4 * P, 1: 2 * P + 2 * S, 2: P + 3 * S, 3: 4 * S}[stage]
+        nbytes = {0: 16 * P, 1: 4 * P + 12 * S, 2: 2 * P + 14 * S, 3: 16 * S}[stage]
+        return values, nbytes
+
+
+def plan(numels, n_ranks: int, align: int = 16, groups=None) -> Plan:
+    """Partition tensors into N owner shards [P1 "Problem"; P2 contiguous
+    gradients; P4 "ZeRO Stages"].  ``groups`` gives each tensor's layer group
+    (non-decreasing from 0, no gaps); each group is planned on its own."""
+    numels = [int(n) for n in numels]
+    if n_ranks < 1 or align < 1 or any(n < 0 for n in numels):
+        raise ValueError("bad plan arguments")
+    if groups is None:
+        groups = [0] * len(numels)
+    groups = [int(g) for g in groups]
+    if len(groups) != len(numels):
+        raise ValueError("one group per tensor")
+    n_groups = (max(groups) + 1) if groups else 1
+    for a, b in zip(groups, groups[1:]):
+        if not (b == a or b == a + 1):
+            raise ValueError("groups must be non-decreasing without gaps")
+    if groups and groups[0] != 0:
+        raise ValueError("groups must start at 0")
+    p = Plan(numels=numels, n_ranks=n_ranks, align=align)
+    quantum = n_ranks * align
+    flat_off = 0
+    rank_off = 0
+    for gi in range(n_groups):
+        members = [t for t, g in enumerate(groups) if g == gi]
+        psi = 0
+        for t in members:
+            p.tensor_group.append(gi)
+            p.tensor_group_off.append(psi)
+            psi += numels[t]
+        psi_pad = -(-psi // quantum) * quantum
+        grp = Group(gi, members, psi, psi_pad, psi_pad // n_ranks, flat_off, rank_off)
+        p.groups.append(grp)
+        flat_off += psi_pad
+        rank_off += grp.shard
+    return p
+
+
+def volume(p: Plan):
+    """Elements each rank sends and receives in one reduce-scatter (and, the
+    same, in one all-gather) over a ring [P3]: (N-1) chunks of S."""
+    per = (p.n_ranks - 1) * p.shard_total
+    return per, per
+
+
+# ---------------------------------------------------------------------------
+# dtype helpers (plain definitions)
+# ---------------------------------------------------------------------------
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> fp32 (exact: the upper half of the fp32 word)."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def f32_to_bf16(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest, ties to even; NaN stays a
+    (quiet) NaN, overflow rounds to infinity."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    is_nan = (u & np.uint64(0x7FFFFFFF)) > np.uint64(0x7F800000)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) & np.uint64(0xFFFF)
+    r = np.where(is_nan, (u >> np.uint64(16)) | np.uint64(0x0040), r)
+    return r.astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# a2: ring reduce-scatter, step by step with mailboxes [P3]
+# ---------------------------------------------------------------------------
+def _chunk(k: int, S: int, a: int, b: int):
+    """Local slice of owner k's chunk inside the window [a, b)."""
+    lo, hi = max(a, k * S), min(b, (k + 1) * S)
+    if hi <= lo:
+        return 0, 0
+    return lo - a, hi - a
+
+
+def ring_reduce_scatter(local, S: int, window=None, narrated: bool = False):
+    """Reduce-scatter N ranks' gradients over a ring.
+
+    ``local[r]`` is rank r's fp32 gradient over the group-local window
+    [a, b) (default: the whole group, a = 0).  Chunk k (the elements owner k
+    keeps, [kS, (k+1)S)) is summed in fp32 as a partial that one rank passes
+    to the next, each receiver adding its own copy of the chunk [P3].
+
+    Returns (reduced, sent, received): reduced[k] is owner k's reduced chunk
+    (window part), sent[r] / received[r] count the elements rank r moved.
+    """
+    n = len(local)
+    a, b = (0, len(local[0])) if window is None else window
+    sent = [0] * n
+    recv = [0] * n
+    if n == 1:
+        lo, hi = _chunk(0, S, a, b)
+        return [local[0][lo:hi].astype(F32, copy=True)], sent, recv
+    if not narrated:
+        # At step s rank r forwards the running partial of chunk (r-1-s) mod N
+        # to rank r+1, which adds its own copy.  The chain of chunk k is
+        # k+1 -> k+2 -> ... -> k, so the owner adds last and keeps the result.
+        holding = [None] * n
+        for s in range(n - 1):
+            mailbox = [None] * n
+            for r in range(n):
+                c = (r - 1 - s) % n
+                lo, hi = _chunk(c, S, a, b)
+                payload = local[r][lo:hi].astype(F32, copy=True) if s == 0 else holding[r]
+                mailbox[(r + 1) % n] = (c, payload)
+                sent[r] += payload.size
+            for r in range(n):
+                c, payload = mailbox[r]
+                lo, hi = _chunk(c, S, a, b)
+                recv[r] += payload.size
+                holding[r] = (payload + local[r][lo:hi]).astype(F32)
+        return holding, sent, recv
+    # Literal narration of [P3]: the chain of chunk k starts at its owner k,
+    # runs k -> k+1 -> ... -> k-1, and the last rank sends the total back.
+    holding = [None] * n
+    final = [None] * n
+    for s in range(n):
+        mailbox = [None] * n
+        for r in range(n):
+            c = (r - s) % n
+            lo, hi = _chunk(c, S, a, b)
+            payload = local[r][lo:hi].astype(F32, copy=True) if s == 0 else holding[r]
+            mailbox[(r + 1) % n] = (c, payload)
+            sent[r] += payload.size
+        for r in range(n):
+            c, payload = mailbox[r]
+            lo, hi = _chunk(c, S, a, b)
+            recv[r] += payload.size
+            if c == r:                      # the total came back to its owner
+                final[r] = payload
+            else:
+                holding[r] = (payload + local[r][lo:hi]).astype(F32)
+    return final, sent, recv
+
+
+def ring_all_gather(shards, S: int, window=None):
+    """All-gather owner shards over a ring [P3]: at step s rank r forwards
+    chunk (r-s) mod N to rank r+1.  ``shards[k]`` is owner k's chunk (window
+    part).  Returns (full buffers of every rank, sent, received)."""
+    n = len(shards)
+    sizes = [len(x) for x in shards]
+    total = sum(sizes)
+    starts = np.cumsum([0] + sizes[:-1]).tolist()
+    have = [dict() for _ in range(n)]
+    for r in range(n):
+        have[r][r] = shards[r]
+    sent = [0] * n
+    recv = [0] * n
+    for s in range(n - 1):
+        mailbox = [None] * n
+        for r in range(n):
+            c = (r - s) % n
+            mailbox[(r + 1) % n] = (c, have[r][c])
+            sent[r] += sizes[c]
+        for r in range(n):
+            c, payload = mailbox[r]
+            have[r][c] = payload.copy()
+            recv[r] += sizes[c]
+    out = []
+    for r in range(n):
+        full = np.empty(total, dtype=shards[0].dtype)
+        for c in range(n):
+            full[starts[c]:starts[c] + sizes[c]] = have[r][c]
+        out.append(full)
+    return out, sent, recv
+
+
+# ---------------------------------------------------------------------------
+# a3: scale and global-norm clip
+# ---------------------------------------------------------------------------
+def scale(reduced, grad_scale):
+    """g = reduced * grad_scale in fp32 (grad_scale = 1/N averages)."""
+    s = F32(grad_scale)
+    return [(x * s).astype(F32) for x in reduced]
+
+
+def grad_norm(g_chunks, max_norm: float):
+    """Global L2 norm of the scaled gradient, accumulated in fp64 over every
+    element in order, and the clip coefficient min(1, max_norm/(norm+1e-6))
+    rounded to fp32 (the coefficient torch.nn.utils.clip_grad_norm_ applies)."""
+    acc = 0.0
+    for x in g_chunks:
+        d = x.astype(np.float64)
+        acc += float(np.dot(d, d))
+    norm = float(np.sqrt(acc))
+    coef = min(1.0, float(max_norm) / (norm + 1e-6))
+    return norm, F32(coef)
+
+
+# ---------------------------------------------------------------------------
+# a4: Adam on the owner's shard [KB Algorithm 1; P4 "Memory Components"]
+# ---------------------------------------------------------------------------
+def bias_corrections(beta1: float, beta2: float, step: int):
+    """1 - beta^t for both moments: beta (an fp32 value) raised to t by t
+    successive fp64 multiplications, subtracted from 1 in fp64, rounded once
+    to fp32."""
+    p1 = 1.0
+    p2 = 1.0
+    b1 = float(F32(beta1))
+    b2 = float(F32(beta2))
+    for _ in range(int(step)):
+        p1 *= b1
+        p2 *= b2
+    return F32(1.0 - p1), F32(1.0 - p2)
+
+
+def adam_update(p, m, v, g, lr, beta1, beta2, eps, weight_decay, step):
+    """One Adam step at step number t (t >= 1), fp32, one rounding per op:
+
+        p  <- p - (lr*wd)*p                       (only when wd != 0)
+        m  <- b1*m + (1-b1)*g
+        v  <- b2*v + (1-b2)*(g*g)
+        mh <- m / bc1 ;  vh <- v / bc2           bc = 1 - beta^t
+        p  <- p - (lr*mh) / (sqrt(vh) + eps)
+
+    Returns new (p, m, v)."""
+    lr, b1, b2, eps, wd = F32(lr), F32(beta1), F32(beta2), F32(eps), F32(weight_decay)
+    omb1 = F32(F32(1.0) - b1)
+    omb2 = F32(F32(1.0) - b2)
+    bc1, bc2 = bias_corrections(b1, b2, step)
+    p = p.astype(F32)
+    if wd != F32(0.0):
+        lrwd = F32(lr * wd)
+        p = (p - (lrwd * p).astype(F32)).astype(F32)
+    m = ((b1 * m).astype(F32) + (omb1 * g).astype(F32)).astype(F32)
+    gg = (g * g).astype(F32)
+    v = ((b2 * v).astype(F32) + (omb2 * gg).astype(F32)).astype(F32)
+    mh = (m / bc1).astype(F32)
+    vh = (v / bc2).astype(F32)
+    denom = (np.sqrt(vh).astype(F32) + eps).astype(F32)
+    upd = ((lr * mh).astype(F32) / denom).astype(F32)
+    p = (p - upd).astype(F32)
+    return p, m, v
+
+
+@dataclass
+class AdamHP:
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+
+
+# ---------------------------------------------------------------------------
+# One ZeRO step (stage 1/2 layout) over a window of one group
+# ---------------------------------------------------------------------------
+def zero_step(local, master, m, v, S: int, step: int, hp: AdamHP, grad_scale=None,
+              window=None, clip_coef=None, out_dtype: str = "bf16", narrated=False):
+    """Reduce-scatter + scale (+ clip) + Adam on each owner's chunk + cast +
+    all-gather [P1 "Problem"; P3].
+
+    ``local[r]``: rank r's fp32 gradient over the window [a, b) of the group
+    (bf16 gradients are converted exactly beforehand); ``master``, ``m``,
+    ``v``: fp32 flat state over the same window (owner k's part is its chunk).
+    ``clip_coef``: an fp32 coefficient computed from the whole gradient, or
+    None.  Returns dict(master, m, v, reduced, full (rank 0's gathered
+    buffer), fulls (every rank's), rs_sent, rs_recv, ag_sent, ag_recv).
+    """
+    n = len(local)
+    a, b = (0, len(local[0])) if window is None else window
+    if grad_scale is None:
+        grad_scale = F32(1.0) / F32(n)
+    reduced, rs_sent, rs_recv = ring_reduce_scatter(local, S, (a, b), narrated)
+    g = scale(reduced, grad_scale)
+    if clip_coef is not None:
+        g = [(x * F32(clip_coef)).astype(F32) for x in g]
+    new_master = master.astype(F32, copy=True)
+    new_m = m.astype(F32, copy=True)
+    new_v = v.astype(F32, copy=True)
+    outs = []
+    for k in range(n):
+        lo, hi = _chunk(k, S, a, b)
+        pk, mk, vk = adam_update(master[lo:hi], m[lo:hi], v[lo:hi], g[k], hp.lr, hp.beta1,
+                                 hp.beta2, hp.eps, hp.weight_decay, step)
+        new_master[lo:hi], new_m[lo:hi], new_v[lo:hi] = pk, mk, vk
+        outs.append(f32_to_bf16(pk) if out_dtype == "bf16" else pk.copy())
+    fulls, ag_sent, ag_recv = ring_all_gather(outs, S)
+    return dict(master=new_master, m=new_m, v=new_v, reduced=reduced, g=g, full=fulls[0],
+                fulls=fulls, rs_sent=rs_sent, rs_recv=rs_recv, ag_sent=ag_sent,
+                ag_recv=ag_recv, shards=outs)
+
+
+def gather_layer(rank_shards):
+    """Stage-3 gather of one layer group [P4 "Implementation Strategy";
+    P2]: every rank contributes its bf16 shard of the group and receives the
+    others' over a ring; returns the contiguous layer buffer (rank 0's copy)
+    and the per-rank counters."""
+    fulls, sent, recv = ring_all_gather(rank_shards, len(rank_shards[0]))
+    return fulls[0], sent, recv
+
+
+def layer_checksum(bits: np.ndarray) -> int:
+    """Checksum a consumer computes over a gathered bf16 layer buffer:
+    sum over j of bits[j] * (1 + (j mod 65536)), mod 2**64."""
+    j = np.arange(bits.size, dtype=np.uint64)
+    w = np.uint64(1) + (j & np.uint64(0xFFFF))
+    with np.errstate(over="ignore"):
+        return int(np.sum(bits.astype(np.uint64) * w, dtype=np.uint64))
