@@ -1,0 +1,422 @@
+"""Benchmark of the ZeRO sharded-optimizer hot path on one GB300 per rank.
+
+Default workload: the GPT-2-small parameter list (124,439,808 parameters, 148
+tensors), N = 8 emulated data-parallel ranks, bf16 gradients, fp32 master /
+m / v, bf16 gathered parameters; one step = one fused zero_step (ring-order
+reduce-scatter + scale + Adam on every owner shard + all-gather).  Prints one
+JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload gpt2-small|gpt2-medium|llama-1.4b|llama-7b-stage3|tiny]
+
+Under torchrun every rank runs an independent replica on its own GPU (the
+method shards nothing across GPUs here); value = all ranks' parameters
+updated / max-over-ranks time.  --impl reference times the CPU oracle on a
+bounded window of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused ZeRO step Gparams/s and achieved HBM GB/s (% of peak), 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------ distributed --
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = torch.device("cuda", self.local_rank) if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict:
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        top = max(sm)
+        loaded = [s for s in sm if s >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers --
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("zero_rs.cu", "zero_device.cuh", "zero_kernels.cu"):
+        with open(os.path.join(ROOT, "zero_sharded_optimizer_device_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, only while the
+    kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload, {}).get(kernel)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("bytes_per_launch")
+
+
+def algorithmic_bytes(n_ranks: int, psi: int, grad_bytes: int) -> int:
+    """Bytes one fused step must move: N gradient reads, 12 B of fp32
+    master/m/v read and 12 B written, 2 B of bf16 parameters written."""
+    return psi * (n_ranks * grad_bytes + 24 + 2)
+
+
+# --------------------------------------------------------- our GPU arm ----
+def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = False) -> dict:
+    import torch
+    import synth
+    import zero_sharded_optimizer_device_gb300 as Z
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    plan = Z.zero_plan(w.numels, w.n_ranks, w.align)
+    info = Z.zero_plan_info(plan)
+    P, N = info["psi_pad"], w.n_ranks
+    gdt = torch.bfloat16 if w.grad_dtype == "bf16" else torch.float32
+    zg = Z.ZERO_BF16 if w.grad_dtype == "bf16" else Z.ZERO_F32
+    gbytes = 2 if w.grad_dtype == "bf16" else 4
+    grads = [torch.empty(P, dtype=gdt, device=dev) for _ in range(N)]
+    for r in range(N):
+        synth.fill_tensor(grads[r], w.seed, synth.GRAD, 1, r, 0, w.grad_sigma, w.psi,
+                          w.heavy_tail)
+    master = torch.empty(P, dtype=torch.float32, device=dev)
+    synth.fill_tensor(master, w.seed, synth.MASTER, 0, 0, 0, w.master_sigma, w.psi)
+    m = torch.zeros_like(master)
+    v = torch.zeros_like(master)
+    out = torch.empty(P, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    t = [0]
+
+    def step():
+        t[0] += 1
+        Z.zero_step(plan, 0, grads, zg, master, m, v, Z.adam_hp(t[0], 1.0 / N), None, out,
+                    Z.ZERO_BF16, stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+
+    if kernel_only:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        return dict(local_ms=ms, launch_ms=ms, e2e_ms=ms, psi=w.psi, psi_pad=P, n_ranks=N,
+                    gbytes=gbytes, copy_gbs=None, clocks={}, h2d=0, d2h=0, e2e_steps=0)
+
+    # copy-kernel peak of this GPU (context for the roofline denominator)
+    cbytes = 2 << 30
+    a = torch.empty(cbytes // 4, dtype=torch.float32, device=dev)
+    b = torch.empty_like(a)
+    for _ in range(3):
+        Z.zero_copy(b, a, cbytes, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(10):
+        Z.zero_copy(b, a, cbytes, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    copy_gbs = 2 * cbytes * 10 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del a, b
+
+    # timed region: K steps, per-launch events on the launching stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+    local_ms = t0.elapsed_time(t1) / steps
+    launch_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+
+    # end to end through the public API: inputs from pinned host memory,
+    # updated bf16 parameters back to pinned host memory, every step
+    h_grads = [torch.empty(P, dtype=gdt, pin_memory=True) for _ in range(N)]
+    for r in range(N):
+        h_grads[r].copy_(grads[r])
+    h_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
+    e2e_steps = max(5, min(50, steps // 20))
+
+    def e2e_step():
+        for r in range(N):
+            grads[r].copy_(h_grads[r], non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+
+    return dict(local_ms=local_ms, launch_ms=launch_ms, e2e_ms=e2e_ms, psi=w.psi, psi_pad=P,
+                n_ranks=N, gbytes=gbytes, copy_gbs=copy_gbs, clocks=clocks.summary(),
+                h2d=N * P * gbytes, d2h=P * 2, e2e_steps=e2e_steps)
+
+
+# ------------------------------------------------- oracle on the host cores --
+def oracle_sample(w, target_s: float, max_steps: int | None = None, window: int | None = None):
+    """Time the CPU oracle's fused step on a window of the workload that
+    straddles the boundary between owners 0 and 1; inputs generated before
+    the clock starts.  Returns (params per second, description, steps)."""
+    import numpy as np
+    import synth
+    from oracle import zero_oracle as O
+
+    p = O.plan(w.numels, w.n_ranks, w.align)
+    S = p.groups[0].shard
+    win = window or min(p.psi_pad, 1 << 20)
+    a = max(0, min(S - win // 2, p.psi_pad - win))
+    b = a + win
+    sdt = synth.DTYPE_BF16 if w.grad_dtype == "bf16" else synth.DTYPE_F32
+    local = []
+    for r in range(w.n_ranks):
+        x = synth.values(w.seed, synth.GRAD, 1, r, a, b, w.grad_sigma, w.psi, w.heavy_tail, sdt)
+        local.append(O.bf16_to_f32(x) if sdt == synth.DTYPE_BF16 else x)
+    master = synth.values(w.seed, synth.MASTER, 0, 0, a, b, w.master_sigma, w.psi)
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    hp = O.AdamHP()
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        steps += 1
+        r = O.zero_step(local, master, m, v, S, steps, hp, window=(a, b))
+        master, m, v = r["master"], r["m"], r["v"]
+        el = time.perf_counter() - t0
+        if (max_steps and steps >= max_steps) or (not max_steps and el >= target_s):
+            break
+    desc = (f"oracle fused step on elements [{a},{b}) of {w.name} (N={w.n_ranks}, owner 0/1 "
+            f"boundary), {steps} steps, single-threaded numpy")
+    return win * steps / el, desc, steps, el
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+# -------------------------------------------------------------------- main --
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gpt2-small")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scale", type=int, default=1,
+                    help="shrink the workload's tensors by this factor (profiling cases)")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time only the step kernel: no copy peak, e2e or CPU baseline")
+    args = ap.parse_args(argv)
+    from synth import workloads as W
+    w = W.ALL[args.workload]
+    if args.scale > 1:
+        w = W.mini(w, scale=args.scale)
+    dist = Dist()
+
+    if args.impl == "reference":
+        if dist.rank != 0:
+            dist.close()
+            return
+        # per step a bounded window, sized so warmup + steps stay ~2 minutes
+        probe_rate, _, _, _ = oracle_sample(w, 0.0, max_steps=1, window=1 << 16)
+        budget = 120.0 / max(1, args.steps + args.warmup)
+        win = int(min(1 << 22, max(1 << 12, probe_rate * budget)))
+        win -= win % 16
+        if args.warmup:
+            oracle_sample(w, 0.0, max_steps=args.warmup, window=win)
+        rate, desc, steps, el = oracle_sample(w, 0.0, max_steps=args.steps, window=win)
+        value = rate / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "Gparams/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": el / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": f"{w.name} fused ZeRO step (oracle window)",
+                           "psi": w.psi, "n_ranks": w.n_ranks, "sample_params": win},
+                "cpu_baseline": {"value": value, "unit": "Gparams/s", "cores": 1,
+                                 "kind": "oracle", "sample": desc, "cpu": cpu_model()},
+                "e2e": {"value": value, "unit": "Gparams/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        dist.close()
+        return
+
+    import torch
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    import zero_sharded_optimizer_device_gb300  # noqa: F401  (fails loudly when unbuilt)
+
+    res = bench_fused(w, args.steps, args.warmup, dist, args.kernel_only)
+    ms = dist.max(res["local_ms"])
+    e2e_ms = dist.max(res["e2e_ms"])
+    n_gpus = dist.world
+    value = n_gpus * w.psi / (ms * 1e-3) / 1e9
+    e2e_value = n_gpus * w.psi / (e2e_ms * 1e-3) / 1e9
+    abytes = algorithmic_bytes(res["n_ranks"], res["psi_pad"], res["gbytes"])
+    peak, peak_kind = measured_hbm_peak()
+    achieved = abytes / (res["launch_ms"] * 1e-3) / 1e9
+    step_gbs = abytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "Gparams/s", "n_gpus": n_gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name} fused zero_step", "psi": w.psi,
+                   "n_ranks": res["n_ranks"], "align": w.align, "grad_dtype": w.grad_dtype,
+                   "state": "fp32 master/m/v", "gathered": "bf16",
+                   "parallelism": f"replicas x{n_gpus} (ranks emulated on each GPU)",
+                   "bytes_per_step": abytes,
+                   "l2": f"inputs {abytes / 1e9:.2f} GB per step > L2 129 MB, no flush"},
+        "hbm_gbs": step_gbs, "hbm_pct_of_peak": 100.0 * step_gbs / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "fused_kernel<8,bf16>",
+                     "algorithmic_bytes_per_launch": abytes,
+                     "traffic": profiled_traffic("fused_kernel", w.name)},
+        "copy_peak_gbs": res["copy_gbs"],
+        "clocks": res["clocks"],
+        "e2e": {"value": e2e_value, "unit": "Gparams/s", "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"], "ms_per_step": e2e_ms,
+                "steps": res["e2e_steps"]},
+        "gpu_launches": args.steps,
+    }
+    if args.kernel_only:
+        line = {"kernel_only": True, "workload": w.name, "psi": w.psi, "ms_per_step": ms,
+                "value": value, "unit": "Gparams/s", "roofline": line["roofline"]}
+    elif dist.rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
+        rate, desc, steps, el = oracle_sample(w, 12.0)
+        line["cpu_baseline"] = {"value": rate / 1e9, "unit": "Gparams/s", "cores": 1,
+                                "kind": "oracle", "sample": desc, "cpu": cpu_model(),
+                                "nproc": os.cpu_count()}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,246 @@
+/*
+ * zero.h -- C ABI of libzero, the data-parallel hot path of ZeRO stages 1-3
+ * on one GPU, with the N data-parallel ranks emulated as N device buffers.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] "[REQUEST] Direct Correspondence between Gradient and Optimizer
+ *        States to Reduce Communication?" (DeepSpeed issue 4582), "Problem":
+ *        gradients are partitioned, reduce-scattered to the owners of the
+ *        optimizer state, the owners update their parameters, and the
+ *        parameters are all-gathered.
+ *   [P2] "Why does not the stage 3 implementation use broadcast and
+ *        reduce-scatter?" (DeepSpeed issue 1173), answers: stage 3 gathers
+ *        parameters with all-gather; the reduce-scatter runs over contiguous
+ *        gradient buffers only.
+ *   [P3] "Why DeepSpeed ZeRO paper says reduce-scatter (or all-gather) has
+ *        data movement of Psi elements?" (DeepSpeed discussion 6594):
+ *        all-reduce = reduce-scatter + all-gather; the ring schedule.
+ *   [P4] "ZeRO Optimizer" (wiki page): "Memory Components", "ZeRO Stages",
+ *        "Implementation Strategy", "Communication Optimization",
+ *        "Theoretical Reductions".
+ *   [KB] Kingma and Ba, "Adam" (2015), Algorithm 1 (the pages name m and v
+ *        but not the update formula).
+ *
+ * Conventions
+ *   - Every function returns an int status: ZERO_OK (0) or a negative
+ *     ZERO_E* code.  No C++ exception crosses this boundary.
+ *   - Plans are opaque host objects owned by the library; free them with
+ *     zero_plan_destroy().  A plan is immutable, so one plan may be used
+ *     from several host threads at once.
+ *   - Every device buffer is allocated and owned by the caller.  No hot call
+ *     allocates device or pinned memory.
+ *   - Device calls are asynchronous on the caller's stream (a cudaStream_t
+ *     passed as zero_stream_t; NULL = the legacy default stream).  They
+ *     report argument errors and launch errors only; a later
+ *     cudaStreamSynchronize reports execution errors.
+ *   - Every device pointer must be 16-byte aligned (ZERO_EALIGN otherwise),
+ *     except fp64 partial sums (8 bytes) and the checksum word (8 bytes).
+ *     Element offsets that break 16-byte vectors (odd windows, align=1
+ *     shards) are handled inside the kernels.
+ *   - Flat arrays ("flat"): reduced gradient, fp32 master, m, v and the full
+ *     gathered parameter buffer.  Each holds psi_pad elements of all groups,
+ *     group g at flat_off(g); inside a group, owner rank r's shard is
+ *     [r*S_g, (r+1)*S_g).  A single-group plan (stages 1 and 2) has
+ *     flat_off = 0, so rank r's shard sits at r*S.
+ *   - Per-rank gradient buffers ("grads"): a host array of N device
+ *     pointers; grads[r] holds rank r's full gradient of ONE group,
+ *     psi_pad(g) elements in group-local order (padding elements must be 0).
+ *   - Per-rank parameter shard buffers ("shards", stage 3): a host array of
+ *     N device pointers; shards[r] holds rank r's bf16 shards of all groups,
+ *     shard_total elements, group g's shard at rank_off(g).
+ *   - Windows [begin, end) are group-local element indices,
+ *     0 <= begin <= end <= psi_pad(g).  Any begin/end is accepted.
+ */
+#ifndef ZERO_H_
+#define ZERO_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO_OK 0
+#define ZERO_EINVAL (-1)   /* null/negative/invalid argument */
+#define ZERO_EALIGN (-2)   /* device pointer not 16-byte aligned */
+#define ZERO_ERANGE (-3)   /* group, rank, tensor or window outside the plan */
+#define ZERO_EDTYPE (-4)   /* dtype not supported by this call */
+#define ZERO_ENOMEM (-5)   /* host allocation failed */
+#define ZERO_ECUDA (-6)    /* CUDA runtime error; see zero_last_cuda_error() */
+#define ZERO_ETIMEOUT (-7) /* a bounded device wait ran out */
+
+#define ZERO_MAX_RANKS 64  /* largest N the kernels accept */
+
+typedef enum { ZERO_F32 = 0, ZERO_BF16 = 1 } zero_dtype_t;
+
+typedef struct zero_plan zero_plan_t;
+typedef void* zero_stream_t; /* a cudaStream_t */
+
+typedef struct {
+  int64_t psi;          /* real parameters, all groups */
+  int64_t psi_pad;      /* padded flat length, all groups */
+  int64_t shard_total;  /* elements each rank owns, all groups (sum of S_g) */
+  int64_t n_tensors;
+  int32_t n_ranks;      /* N */
+  int32_t align;        /* shard size and start quantum, in elements */
+  int32_t n_groups;
+  int32_t reserved;
+} zero_plan_info_t;
+
+typedef struct {
+  int64_t psi, psi_pad, shard; /* S_g = psi_pad / N */
+  int64_t flat_off;            /* group start in flat arrays */
+  int64_t rank_off;            /* group start in each rank's shard buffer */
+  int64_t first_tensor, n_tensors;
+} zero_group_info_t;
+
+typedef struct {
+  int64_t tensor;      /* tensor index */
+  int64_t tensor_off;  /* first element of the piece inside the tensor */
+  int64_t flat_off;    /* its flat index */
+  int64_t len;         /* elements */
+} zero_seg_t;
+
+typedef struct {
+  int64_t values; /* [P4 "Theoretical Reductions"] values per device */
+  int64_t bytes;  /* bf16 params and grads, fp32 master + m + v */
+} zero_mem_t;
+
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+  float grad_scale; /* multiplies the reduced sum; 1/N averages */
+  int64_t step;     /* t >= 1: this update's step number */
+} zero_adam_t;
+
+/* ------------------------------------------------------------- library -- */
+int zero_version(void);
+/* Text for a status code; a static string, never NULL. */
+const char* zero_strerror(int status);
+/* The cudaError_t of the last ZERO_ECUDA returned on this host thread. */
+int zero_last_cuda_error(void);
+
+/* ----------------------------------------------------------------- plan --
+ * zero_plan: partition a list of tensors into N owner shards [P1
+ * "Problem"; P2: one contiguous gradient buffer; P4 "ZeRO Stages"].
+ * The tensors are concatenated in list order with no per-tensor padding.
+ * Each group is padded at its tail to psi_pad(g) = ceil(psi(g)/(N*align))
+ * * N*align and cut into N equal shards S_g = psi_pad(g)/N; rank r owns
+ * [r*S_g, (r+1)*S_g).  group_of_tensor (may be NULL = one group) gives each
+ * tensor's layer group; it must start at 0 and be non-decreasing without
+ * gaps (stage 3 plans every layer group on its own [P4 "Implementation
+ * Strategy"]).  numels[t] >= 0; 1 <= N <= 64; align >= 1.
+ * Errors: ZERO_EINVAL (bad arguments or group list, size overflow),
+ * ZERO_ENOMEM.  *out is set only on success. */
+int zero_plan(const int64_t* numels, int64_t n_tensors, int32_t n_ranks, int32_t align,
+              const int32_t* group_of_tensor, zero_plan_t** out);
+int zero_plan_destroy(zero_plan_t* plan);
+int zero_plan_info(const zero_plan_t* plan, zero_plan_info_t* out);
+int zero_plan_group(const zero_plan_t* plan, int32_t group, zero_group_info_t* out);
+/* Flat offset of tensor t and the ranks owning its first and last element
+ * (-1 for an empty tensor). */
+int zero_plan_tensor(const zero_plan_t* plan, int64_t t, int64_t* flat_off,
+                     int32_t* first_owner, int32_t* last_owner);
+/* Rank r's shard of group g: flat begin, length S_g, real (non-padding)
+ * elements. */
+int zero_plan_shard(const zero_plan_t* plan, int32_t group, int32_t rank, int64_t* begin,
+                    int64_t* len, int64_t* valid_len);
+/* Pieces of tensors rank r owns, in flat order.  Writes min(cap, count)
+ * entries to out (out may be NULL when cap == 0); *n = count. */
+int zero_plan_segments(const zero_plan_t* plan, int32_t rank, zero_seg_t* out, int64_t cap,
+                       int64_t* n);
+/* Per-device memory of stage 0 (plain data parallelism: 4P values [P4
+ * "Memory Components"]), 1 (2P + 2P/N), 2 (P + 3P/N) or 3 (4P/N) [P4
+ * "Theoretical Reductions"], with P = psi_pad and P/N = shard_total; bytes
+ * count bf16 params and grads and 12 bytes of fp32 master + m + v. */
+int zero_plan_memory(const zero_plan_t* plan, int32_t stage, zero_mem_t* out);
+/* Elements each rank sends and receives in one ring reduce-scatter (and in
+ * one all-gather): (N-1) * shard_total [P3]. */
+int zero_plan_volume(const zero_plan_t* plan, int64_t* send_per_rank, int64_t* recv_per_rank);
+
+/* ------------------------------------------------------- device calls -- */
+
+/* zero_reduce_scatter [P1 "Problem"; P3]: for every i in [begin, end) of
+ * group g, reduced[flat_off(g) + i] = the fp32 sum of grads[r][i] over the
+ * N ranks, in the ring order of owner k = i / S_g: k+1, k+2, ..., N-1, 0,
+ * ..., k (the owner adds last).  gdtype: ZERO_F32 or ZERO_BF16.
+ * If sumsq_partials is not NULL, also writes zero_rs_partials() fp64
+ * partial sums of (reduced * grad_scale)^2 over the window, for
+ * zero_grad_norm().  Errors: EINVAL, EALIGN, ERANGE, EDTYPE, ECUDA. */
+int zero_reduce_scatter(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                        zero_dtype_t gdtype, float* reduced, int64_t begin, int64_t end,
+                        float grad_scale, double* sumsq_partials, zero_stream_t stream);
+/* Number of fp64 partials zero_reduce_scatter writes for a window of
+ * n_elements with this plan's N and gdtype on the current device (one per
+ * block of its launch; blocks without work write 0). */
+int zero_rs_partials(const zero_plan_t* plan, zero_dtype_t gdtype, int64_t n_elements,
+                     int64_t* n_partials);
+
+/* zero_grad_norm: norm = sqrt(sum of n fp64 partials), summed in a fixed
+ * order; coef = min(1, max_norm / (norm + 1e-6)) rounded to fp32.  Writes
+ * *d_norm (fp32) and *d_coef (fp32) on the device; either may be NULL.
+ * The clip is not on the pages; it is the coefficient torch's
+ * clip_grad_norm_ applies. */
+int zero_grad_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
+                   float* d_coef, zero_stream_t stream);
+
+/* zero_adam_shard [P1 "Problem"; P4 "Memory Components"; KB]: for i in
+ * [begin, end) of group g (flat index f = flat_off(g) + i):
+ *   grad = reduced[f] * grad_scale (* *d_coef when d_coef != NULL)
+ *   p -= (lr*wd)*p (when wd != 0);  m = b1*m + (1-b1)*grad;
+ *   v = b2*v + (1-b2)*grad^2;  p -= (lr * (m/bc1)) / (sqrt(v/bc2) + eps)
+ * in fp32, one rounding per operation, bc = 1 - beta^t computed in fp64 on
+ * the host and rounded to fp32.  If out != NULL also writes out[f] =
+ * cast(p) (out_dtype ZERO_BF16: round to nearest even; ZERO_F32: copy).
+ * Errors: EINVAL, EALIGN, ERANGE, EDTYPE, ECUDA. */
+int zero_adam_shard(const zero_plan_t* plan, int32_t group, float* master, float* m, float* v,
+                    const float* reduced, const zero_adam_t* hp, const float* d_coef,
+                    int64_t begin, int64_t end, void* out, zero_dtype_t out_dtype,
+                    zero_stream_t stream);
+
+/* zero_all_gather [P1 "Problem"; P3 all-gather]: full_out[f] = cast(
+ * master[f]) for every element of group g (g = -1: all groups), i.e. every
+ * owner's updated shard lands in the one full flat parameter buffer all
+ * ranks share.  out_dtype: ZERO_BF16 (round to nearest even) or ZERO_F32. */
+int zero_all_gather(const zero_plan_t* plan, int32_t group, const float* master,
+                    void* full_out, zero_dtype_t out_dtype, zero_stream_t stream);
+
+/* zero_step: the fused reduce-scatter + scale (+ clip by *d_coef) + Adam +
+ * all-gather of group g in one pass; the reduced gradient never reaches
+ * memory.  Same arithmetic, per element, as zero_reduce_scatter followed by
+ * zero_adam_shard with out = full_out (bit-identical results).  full_out
+ * may be NULL (no gather). */
+int zero_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
+              zero_dtype_t gdtype, float* master, float* m, float* v, const zero_adam_t* hp,
+              const float* d_coef, void* full_out, zero_dtype_t out_dtype,
+              zero_stream_t stream);
+
+/* zero_step_group (stage 3) [P4 "ZeRO Stages", stage 3]: as zero_step, but
+ * each owner writes its updated bf16 parameters only into its own shard
+ * buffer: shards[k][rank_off(g) + (i - k*S_g)] for owner k of element i. */
+int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                    zero_dtype_t gdtype, float* master, float* m, float* v,
+                    const zero_adam_t* hp, const float* d_coef, void* const* shards,
+                    zero_stream_t stream);
+
+/* zero_gather_layer (stage 3) [P4 "Implementation Strategy": gather a
+ * layer's parameters just before use; P2: by all-gather]: layer_out[j] =
+ * shards[j / S_g][rank_off(g) + j % S_g] for j in [0, psi_pad(g)): the N
+ * ranks' shards of group g concatenated into one contiguous layer buffer.
+ * dtype: element type of the shard buffers (ZERO_BF16 or ZERO_F32). */
+int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
+                      zero_dtype_t dtype, void* layer_out, zero_stream_t stream);
+
+/* zero_layer_checksum: stands in for the layer computation that consumes a
+ * gathered buffer: *d_out = sum over j < n of bits[j] * (1 + j mod 65536)
+ * mod 2^64, over n bf16 bit patterns. */
+int zero_layer_checksum(const void* layer, int64_t n, uint64_t* d_out, zero_stream_t stream);
+
+/* zero_copy: device-to-device copy of `bytes` (a multiple of 16) with
+ * 16-byte loads and stores; measures the achievable HBM copy bandwidth. */
+int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_H_ */

@@ -1,0 +1,173 @@
+"""CPU-only checks of the C ABI: the library loads and exports every function
+include/zero.h declares; the host planner matches the oracle's plan exactly;
+argument checks return their error codes before any device work; host-side
+fault injection; the benchmark's multi-rank aggregation over gloo."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+from oracle import zero_oracle as O
+from synth import workloads as W
+
+Z = pytest.importorskip("zero_sharded_optimizer_device_gb300")
+
+
+def test_library_exports_every_declared_function():
+    lib = Z.binding._lib()
+    declared = Z.header_functions()
+    assert len(declared) >= 20
+    for name in declared:
+        assert hasattr(lib, name), name
+    # and the binding wraps each of them under the same name
+    for name in declared:
+        assert callable(getattr(Z, name)), name
+
+
+def test_strerror_covers_every_status():
+    for code in range(0, -8, -1):
+        assert Z.zero_strerror(code) and Z.zero_strerror(code) != "unknown status"
+    assert Z.zero_strerror(-99) == "unknown status"
+
+
+def _compare_plans(numels, n, align, groups=None):
+    p = Z.zero_plan(numels, n, align, groups)
+    o = O.plan(numels, n, align, groups)
+    info = Z.zero_plan_info(p)
+    assert (info["psi"], info["psi_pad"], info["shard_total"]) == (o.psi, o.psi_pad, o.shard_total)
+    assert info["n_groups"] == len(o.groups)
+    for gi, g in enumerate(o.groups):
+        zg = Z.zero_plan_group(p, gi)
+        assert (zg["psi"], zg["psi_pad"], zg["shard"], zg["flat_off"], zg["rank_off"]) == \
+            (g.psi, g.psi_pad, g.shard, g.flat_off, g.rank_off)
+        for r in range(n):
+            assert Z.zero_plan_shard(p, gi, r) == o.shard_range(gi, r)
+    for t in range(len(numels)):
+        assert Z.zero_plan_tensor(p, t) == (o.tensor_flat_off(t), *o.owner_span(t))
+    for r in range(n):
+        assert Z.zero_plan_segments(p, r) == o.segments(r)
+    for stage in range(4):
+        assert Z.zero_plan_memory(p, stage) == o.memory(stage)
+    assert Z.zero_plan_volume(p) == O.volume(o)
+
+
+@pytest.mark.parametrize("w", list(W.ALL.values()), ids=lambda w: w.name)
+def test_planner_matches_oracle_on_workloads(w):
+    _compare_plans(w.numels, w.n_ranks, w.align, w.groups)
+
+
+@pytest.mark.parametrize("numels,n,align,groups", [
+    ([], 4, 16, None), ([0, 5, 0], 2, 1, None), ([7], 1, 1, None), ([1], 64, 1, None),
+    ([3, 1, 4, 1, 5, 9, 2, 6], 3, 5, [0, 0, 1, 1, 1, 2, 3, 3]), ([10**12, 7], 64, 128, None),
+])
+def test_planner_matches_oracle_on_edge_cases(numels, n, align, groups):
+    _compare_plans(numels, n, align, groups)
+
+
+def test_plan_argument_errors():
+    for args in [([4], 0, 1), ([4], 65, 1), ([4], 2, 0), ([-1], 2, 1)]:
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_plan(*args)
+        assert e.value.status == Z.ZERO_EINVAL
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_plan([4, 4], 2, 1, [0, 2])
+    assert e.value.status == Z.ZERO_EINVAL
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_plan([2 ** 62, 2 ** 62], 2, 1)
+    assert e.value.status == Z.ZERO_EINVAL
+    p = Z.zero_plan([10], 2, 1)
+    for f, a in [(Z.zero_plan_group, (1,)), (Z.zero_plan_shard, (0, 2)),
+                 (Z.zero_plan_tensor, (1,)), (Z.zero_plan_memory, (4,))]:
+        with pytest.raises(Z.ZeroError) as e:
+            f(p, *a)
+        assert e.value.status == Z.ZERO_ERANGE
+
+
+def test_device_call_argument_errors_return_before_any_launch():
+    """Rejected calls never reach the GPU: fake (never dereferenced)
+    addresses suffice, and the status names the first bad argument."""
+    p = Z.zero_plan([100], 4, 1)
+    A = 0x10000                      # 16-byte aligned fake address
+    good = [A] * 4
+    hp = Z.adam_hp(1, 0.25)
+    E = Z.ZeroError
+
+    def status(fn, *a):
+        with pytest.raises(E) as e:
+            fn(*a, stream=0)
+        return e.value.status
+
+    assert status(Z.zero_reduce_scatter, p, 1, good, Z.ZERO_BF16, A, 0, 4, 1.0) == Z.ZERO_ERANGE
+    assert status(Z.zero_reduce_scatter, p, 0, good, 7, A, 0, 4, 1.0) == Z.ZERO_EDTYPE
+    assert status(Z.zero_reduce_scatter, p, 0, good, Z.ZERO_BF16, A, 5, 4, 1.0) == Z.ZERO_ERANGE
+    assert status(Z.zero_reduce_scatter, p, 0, good, Z.ZERO_BF16, A, 0, 101, 1.0) == Z.ZERO_ERANGE
+    assert status(Z.zero_reduce_scatter, p, 0, [A, A, A, A + 8], Z.ZERO_BF16, A, 0, 4,
+                  1.0) == Z.ZERO_EALIGN
+    assert status(Z.zero_reduce_scatter, p, 0, [A, A, 0, A], Z.ZERO_BF16, A, 0, 4,
+                  1.0) == Z.ZERO_EINVAL
+    assert status(Z.zero_reduce_scatter, p, 0, good, Z.ZERO_BF16, A + 4, 0, 4, 1.0) == Z.ZERO_EALIGN
+    assert status(Z.zero_step, p, 0, good, Z.ZERO_BF16, A, A, A + 2, hp, None, A) == Z.ZERO_EALIGN
+    assert status(Z.zero_step, p, 0, good, Z.ZERO_BF16, A, A, A, Z.adam_hp(0, 0.25), None,
+                  A) == Z.ZERO_EINVAL
+    assert status(Z.zero_step, p, 0, good, Z.ZERO_BF16, A, A, A,
+                  Z.adam_hp(1, 0.25, beta1=1.0), None, A) == Z.ZERO_EINVAL
+    assert status(Z.zero_step, p, 0, good, Z.ZERO_BF16, A, A, A,
+                  Z.adam_hp(1, 0.25, lr=float("nan")), None, A) == Z.ZERO_EINVAL
+    assert status(Z.zero_step, p, 0, good, Z.ZERO_BF16, A, A, A, hp, None, A, 9) == Z.ZERO_EDTYPE
+    assert status(Z.zero_step_group, p, 0, good, Z.ZERO_BF16, A, A, A, hp, None,
+                  [A, A, A, 0]) == Z.ZERO_EINVAL
+    assert status(Z.zero_adam_shard, p, 0, A, A, A, A, hp, None, 0, 200, None) == Z.ZERO_ERANGE
+    assert status(Z.zero_all_gather, p, 3, A, A) == Z.ZERO_ERANGE
+    assert status(Z.zero_gather_layer, p, 0, good, Z.ZERO_BF16, A + 1) == Z.ZERO_EALIGN
+    assert status(Z.zero_grad_norm, A, 4, 0.0, None, None) == Z.ZERO_EINVAL
+    assert status(Z.zero_layer_checksum, A, 10, A + 4) == Z.ZERO_EALIGN
+    assert status(Z.zero_copy, A, A, 15) == Z.ZERO_EINVAL
+
+
+def test_rs_partials_requires_known_dtype():
+    p = Z.zero_plan([100], 4, 1)
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_rs_partials(p, 5, 100)
+    assert e.value.status == Z.ZERO_EDTYPE
+
+
+def test_host_fault_injection_reports_enomem():
+    code = ("import os, zero_sharded_optimizer_device_gb300 as Z\n"
+            "try:\n    Z.zero_plan([4], 2, 1)\nexcept Z.ZeroError as e:\n"
+            "    print(e.status)\n")
+    env = dict(os.environ, ZERO_FAULT_INJECT="plan_alloc",
+               PYTHONPATH=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
+    assert out.stdout.strip() == str(Z.ZERO_ENOMEM), out.stderr
+
+
+def _gloo_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    d = bench.Dist()
+    d.barrier()
+    got = d.max(float(10 + rank))
+    d.close()
+    q.put((rank, got))
+
+
+def test_bench_max_over_ranks_with_gloo():
+    """The replicas path: every rank's timing reduced with MAX over a 2-rank
+    gloo group (the same code torchrun drives on GPUs)."""
+    import multiprocessing as mp
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_gloo_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    assert res == {0: 11.0, 1: 11.0}

@@ -1,0 +1,308 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, element by
+element, on seeded inputs: small workloads in full, edge cases, and the
+GPT-2-small workload at full size on sampled windows."""
+import numpy as np
+import pytest
+
+import synth
+from synth import workloads as W
+from oracle import zero_oracle as O
+
+from harness import Case, assert_bf16, assert_close_f32, bits_of
+
+pytestmark = pytest.mark.gpu
+
+
+def _fused_steps(case: Case, steps: int, out_dtype: str = "bf16", group: int = 0):
+    import torch
+    Z = case.Z
+    g = case.groups[group]
+    tdt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+    out = torch.zeros(case.info["psi_pad"], dtype=tdt, device=case.dev)
+    zdt = Z.ZERO_BF16 if out_dtype == "bf16" else Z.ZERO_F32
+    grads = None
+    last = None
+    for s in range(1, steps + 1):
+        grads = case.grads_dev(group, s, grads)
+        Z.zero_step(case.plan, group, grads, case.zdtype, case.master, case.m, case.v,
+                    case.hp_dev(s), None, out, zdt)
+        last = case.oracle_step(group, s, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    f0 = g["flat_off"]
+    sl = slice(f0, f0 + g["psi_pad"])
+    if out_dtype == "bf16":
+        assert_bf16(bits_of(out[sl]), last["full"], "gathered bf16")
+    else:
+        assert_close_f32(out[sl].cpu().numpy(), last["full"], "gathered fp32")
+    return out
+
+
+# ------------------------------------------------------------------- tiny --
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_tiny_fused_three_steps(cuda, out_dtype):
+    w = W.TINY
+    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed)
+    _fused_steps(c, 3, out_dtype)
+    c.check_state("tiny fused")
+    # padding stays exactly zero
+    assert not c.master[w.psi:].any().item()
+
+
+def test_tiny_unfused_chain(cuda):
+    import torch
+    w = W.TINY
+    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed)
+    Z = c.Z
+    P = c.info["psi_pad"]
+    reduced = torch.empty(P, dtype=torch.float32, device=cuda)
+    out32 = torch.empty(P, dtype=torch.float32, device=cuda)
+    out16 = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    for s in range(1, 4):
+        grads = c.grads_dev(0, s)
+        Z.zero_reduce_scatter(c.plan, 0, grads, Z.ZERO_F32, reduced, 0, P, 1.0 / w.n_ranks)
+        Z.zero_adam_shard(c.plan, 0, c.master, c.m, c.v, reduced, c.hp_dev(s), None, 0, P,
+                          None)
+        Z.zero_all_gather(c.plan, 0, c.master, out32, Z.ZERO_F32)
+        Z.zero_all_gather(c.plan, -1, c.master, out16, Z.ZERO_BF16)
+        r = c.oracle_step(0, s, out_dtype="f32")
+        torch.cuda.synchronize()
+        assert_close_f32(reduced.cpu().numpy(), np.concatenate(r["reduced"]), f"reduced s{s}")
+    c.check_state("tiny unfused")
+    assert_close_f32(out32.cpu().numpy(), r["full"], "fp32 gather")
+    assert_bf16(bits_of(out16), O.f32_to_bf16(r["full"]), "bf16 gather")
+
+
+# ------------------------------------------------------ minis of workloads --
+@pytest.mark.parametrize("name,scale,steps", [("gpt2-small", 256, 2), ("gpt2-medium", 1024, 2)])
+def test_mini_fused(cuda, name, scale, steps):
+    w = W.mini(W.ALL[name], scale=scale)
+    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed)
+    _fused_steps(c, steps)
+    c.check_state(w.name)
+
+
+def test_llama_mini_bucketed_with_clip(cuda):
+    import torch
+    w = W.mini(W.LLAMA_1_4B, scale=1024)
+    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed,
+             heavy_tail=True)
+    Z = c.Z
+    P = c.info["psi_pad"]
+    bucket, chunk = 100_003, 400_001       # ragged windows on purpose
+    windows = [(a, min(P, a + bucket)) for a in range(0, P, bucket)]
+    npart = [Z.zero_rs_partials(c.plan, Z.ZERO_BF16, b - a) for a, b in windows]
+    partials = torch.zeros(sum(npart), dtype=torch.float64, device=cuda)
+    reduced = torch.empty(P, dtype=torch.float32, device=cuda)
+    norm = torch.zeros(1, dtype=torch.float32, device=cuda)
+    coef = torch.zeros(1, dtype=torch.float32, device=cuda)
+    out = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    for s in (1, 2):
+        grads = c.grads_dev(0, s)
+        off = 0
+        for (a, b), k in zip(windows, npart):
+            Z.zero_reduce_scatter(c.plan, 0, grads, Z.ZERO_BF16, reduced, a, b, 1.0 / w.n_ranks,
+                                  partials[off:off + k])
+            off += k
+        Z.zero_grad_norm(partials, off, 1.0, norm, coef)
+        for a in range(0, P, chunk):
+            Z.zero_adam_shard(c.plan, 0, c.master, c.m, c.v, reduced, c.hp_dev(s), coef, a,
+                              min(P, a + chunk), out, Z.ZERO_BF16)
+        # oracle: reduce-scatter, global norm, clip coefficient, step
+        local = c.grads_host(0, s)
+        red, _, _ = O.ring_reduce_scatter(local, c.groups[0]["shard"])
+        onorm, ocoef = O.grad_norm(O.scale(red, np.float32(1.0) / np.float32(w.n_ranks)), 1.0)
+        r = c.oracle_step(0, s, clip_coef=ocoef)
+        torch.cuda.synchronize()
+        assert abs(norm.item() - onorm) <= 1e-6 * onorm, (norm.item(), onorm)
+        assert abs(coef.item() - float(ocoef)) <= 1e-6 * float(ocoef)
+        assert float(ocoef) < 1.0      # heavy tails: the clip is active
+        assert_close_f32(reduced.cpu().numpy(), np.concatenate(red), "reduced")
+        # the coefficient may differ in its last bit (fp64 sums in another order)
+        exact = coef.item() == float(ocoef)
+        c.check_state(f"llama mini step {s}", exact=exact)
+        assert_bf16(bits_of(out), r["full"], "gathered", exact=exact)
+
+
+def test_stage3_mini_step_gather_checksum(cuda):
+    import torch
+    # Llama-shaped stage-3 list, scaled down: embedding, two blocks, head
+    d, ffn, vocab = 64, 172, 500
+    blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(2)]
+    numels = [vocab * d] + blocks[0] + blocks[1] + [d, vocab * d]
+    groups = [0] + [1] * 9 + [2] * 9 + [3, 3]
+    c = Case(numels, 16, 16, "bf16", seed=77, groups=groups)
+    Z = c.Z
+    N = 16
+    shards = [torch.zeros(c.info["shard_total"], dtype=torch.bfloat16, device=cuda)
+              for _ in range(N)]
+    for gi in reversed(range(len(c.groups))):
+        grads = c.grads_dev(gi, 1)
+        Z.zero_step_group(c.plan, gi, grads, Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(1), None,
+                          shards)
+        c.oracle_step(gi, 1)
+    torch.cuda.synchronize()
+    c.check_state("stage3")
+    sums = torch.zeros(len(c.groups), dtype=torch.int64, device=cuda)
+    for gi, g in enumerate(c.groups):
+        layer = torch.empty(g["psi_pad"], dtype=torch.bfloat16, device=cuda)
+        Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, layer)
+        Z.zero_layer_checksum(layer, g["psi_pad"], sums[gi:gi + 1])
+        torch.cuda.synchronize()
+        # oracle: each owner's shard is the bf16 cast of its updated master
+        f0, S = g["flat_off"], g["shard"]
+        own = [O.f32_to_bf16(c.h_master[f0 + k * S:f0 + (k + 1) * S]) for k in range(N)]
+        want, sent, recv = O.gather_layer(own)
+        assert_bf16(bits_of(layer), want, f"layer {gi}")
+        for k in range(N):
+            ro = g["rank_off"]
+            assert_bf16(bits_of(shards[k][ro:ro + S]), own[k], f"shard {k} group {gi}")
+        assert sums[gi].item() % (1 << 64) == O.layer_checksum(want) % (1 << 64) or \
+            (sums[gi].item() + (1 << 64)) == O.layer_checksum(want)
+
+
+# ------------------------------------------------------------- edge cases --
+@pytest.mark.parametrize("numels,n,align,gd", [
+    ([37], 1, 1, "f32"),                 # one rank: the reduce is a copy
+    ([1000, 333, 17], 3, 1, "bf16"),     # generic-N kernel, ragged shards
+    ([5, 7, 11, 2001], 5, 3, "f32"),     # shards cut every vector
+    ([4096 * 3 + 5], 64, 1, "bf16"),     # N = 64, S not a multiple of 8
+    ([8, 8], 2, 8, "bf16"),              # tiny, exactly one vector per shard
+    ([10_000, 77], 16, 16, "bf16"),
+])
+def test_edge_shapes_fused_and_unfused(cuda, numels, n, align, gd):
+    import torch
+    c = Case(numels, n, align, gd, seed=sum(numels) + n)
+    Z = c.Z
+    P = c.info["psi_pad"]
+    out = torch.zeros(P, dtype=torch.bfloat16, device=cuda)
+    grads = c.grads_dev(0, 1)
+    Z.zero_step(c.plan, 0, grads, c.zdtype, c.master, c.m, c.v, c.hp_dev(1), None, out,
+                Z.ZERO_BF16)
+    r = c.oracle_step(0, 1)
+    torch.cuda.synchronize()
+    c.check_state(f"edge {numels} N={n}")
+    assert_bf16(bits_of(out), r["full"], "edge gather")
+    # unfused over odd windows reproduces the fused state bit for bit
+    master2, m2, v2 = (torch.empty_like(c.master) for _ in range(3))
+    master2.copy_(c.master)
+    m2.copy_(c.m)
+    v2.copy_(c.v)
+    reduced = torch.zeros(P, dtype=torch.float32, device=cuda)
+    grads = c.grads_dev(0, 2)
+    cuts = sorted({0, P, P // 3 + 1, (2 * P) // 3 - 3, min(P, 9)})
+    for a, b in zip(cuts, cuts[1:]):
+        Z.zero_reduce_scatter(c.plan, 0, grads, c.zdtype, reduced, a, b, 1.0 / n)
+        Z.zero_adam_shard(c.plan, 0, master2, m2, v2, reduced, c.hp_dev(2), None, a, b, None)
+    Z.zero_step(c.plan, 0, grads, c.zdtype, c.master, c.m, c.v, c.hp_dev(2), None, out,
+                Z.ZERO_BF16)
+    c.oracle_step(0, 2)
+    torch.cuda.synchronize()
+    c.check_state("edge step 2")
+    assert torch.equal(master2, c.master) and torch.equal(m2, c.m) and torch.equal(v2, c.v)
+
+
+def test_weight_decay_and_fp32_grads_n8(cuda):
+    hp = O.AdamHP(lr=3e-3, weight_decay=0.05)
+    c = Case([20_000, 3_003], 8, 16, "f32", grad_sigma=1e-2, seed=5, hp=hp)
+    _fused_steps(c, 3)
+    c.check_state("wd fp32")
+
+
+def test_multi_group_unaligned_group_offsets(cuda):
+    # N*align = 3: group offsets are not multiples of 8 elements, so the
+    # flat-array vectors fall back to element accesses
+    import torch
+    c = Case([50, 61, 70, 9], 3, 1, "bf16", seed=9, groups=[0, 1, 1, 2])
+    assert any(g["flat_off"] % 8 for g in c.groups)
+    out = torch.zeros(c.info["psi_pad"], dtype=torch.bfloat16, device=cuda)
+    Z = c.Z
+    for gi in range(len(c.groups)):
+        Z.zero_step(c.plan, gi, c.grads_dev(gi, 1), Z.ZERO_BF16, c.master, c.m, c.v,
+                    c.hp_dev(1), None, out, Z.ZERO_BF16)
+        c.oracle_step(gi, 1)
+    torch.cuda.synchronize()
+    c.check_state("multi-group")
+    assert_bf16(bits_of(out), O.f32_to_bf16(c.h_master), "multi-group gather")
+
+
+def test_empty_plan_and_empty_window_are_noops(cuda):
+    import torch
+    import zero_sharded_optimizer_device_gb300 as Z
+    p = Z.zero_plan([], 4, 16)
+    x = torch.zeros(16, device=cuda)
+    grads = [torch.zeros(16, device=cuda) for _ in range(4)]
+    Z.zero_step(p, 0, grads, Z.ZERO_F32, x, x, x, Z.adam_hp(1, 0.25), None, None)
+    c = Case([100], 4, 1, "f32", seed=3)
+    before = c.master.clone()
+    red = torch.full((c.info["psi_pad"],), 7.0, device=cuda)
+    Z.zero_reduce_scatter(c.plan, 0, c.grads_dev(0, 1), Z.ZERO_F32, red, 50, 50, 0.25)
+    Z.zero_adam_shard(c.plan, 0, c.master, c.m, c.v, red, c.hp_dev(1), None, 10, 10, None)
+    torch.cuda.synchronize()
+    assert torch.equal(before, c.master) and bool((red == 7.0).all())
+
+
+def test_outputs_stay_inside_their_buffers(cuda):
+    """Guard bands: 256 canary bytes before and after every output buffer
+    stay untouched by every call."""
+    import torch
+    c = Case([1000, 337], 4, 1, "bf16", seed=21)
+    Z = c.Z
+    P = c.info["psi_pad"]
+    G = 64  # canary floats on each side
+
+    def guarded(n, dtype):
+        words = (n * (2 if dtype == torch.bfloat16 else 4) + 3) // 4
+        buf = torch.full((words + 2 * G,), -12345.0, dtype=torch.float32, device=cuda)
+        inner = buf[G:G + words].view(dtype)[:n]
+        return buf, inner
+
+    bufs = {}
+    bufs["master"], master = guarded(P, torch.float32)
+    bufs["m"], m = guarded(P, torch.float32)
+    bufs["v"], v = guarded(P, torch.float32)
+    bufs["red"], red = guarded(P, torch.float32)
+    bufs["out"], out = guarded(P, torch.bfloat16)
+    master.copy_(c.master)
+    m.zero_()
+    v.zero_()
+    grads = c.grads_dev(0, 1)
+    Z.zero_reduce_scatter(c.plan, 0, grads, Z.ZERO_BF16, red, 3, P - 5, 0.25)
+    Z.zero_step(c.plan, 0, grads, Z.ZERO_BF16, master, m, v, c.hp_dev(1), None, out, Z.ZERO_BF16)
+    Z.zero_adam_shard(c.plan, 0, master, m, v, red, c.hp_dev(2), None, 1, P - 1, out, Z.ZERO_BF16)
+    Z.zero_all_gather(c.plan, 0, master, out, Z.ZERO_BF16)
+    torch.cuda.synchronize()
+    for name, b in bufs.items():
+        assert bool((b[:G] == -12345.0).all()) and bool((b[-G:] == -12345.0).all()), name
+
+
+# ------------------------------------------------ full size, sampled windows --
+def _sample_windows(P, S, N, half=4096):
+    ws = [(0, 2 * half), (P - 2 * half, P)]
+    for k in range(1, N):
+        ws.append((k * S - half, k * S + half))
+    return ws
+
+
+def test_gpt2_small_full_size_sampled(cuda):
+    """The workload the benchmark times (fused zero_step, N=8, bf16 grads),
+    5 steps at full size; sampled windows across every owner boundary are
+    recomputed by the oracle from generated inputs."""
+    import torch
+    w = W.GPT2_SMALL
+    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed)
+    Z = c.Z
+    P, S = c.info["psi_pad"], c.groups[0]["shard"]
+    assert P == 124_439_808 and S == 15_554_976
+    out = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    grads = None
+    for s in range(1, w.steps + 1):
+        grads = c.grads_dev(0, s, grads)
+        Z.zero_step(c.plan, 0, grads, Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(s), None, out,
+                    Z.ZERO_BF16)
+    torch.cuda.synchronize()
+    for a, b in _sample_windows(P, S, w.n_ranks):
+        last = None
+        for s in range(1, w.steps + 1):
+            last = c.oracle_step(0, s, window=(a, b))
+        c.check_state(f"gpt2-small [{a},{b})", sl=slice(a, b))
+        assert_bf16(bits_of(out[a:b]), last["full"], f"gathered [{a},{b})")

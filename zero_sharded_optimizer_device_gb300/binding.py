@@ -1,0 +1,314 @@
+"""Thin Python binding of libzero (argument marshalling only).
+
+Every function has the name and argument order of its C entry point in
+``include/zero.h``; device buffers may be given as torch tensors, raw
+integer device addresses or None (NULL).  Streams default to torch's current
+CUDA stream.  A non-zero status raises ``ZeroError``.  All computation happens
+in the library's CUDA kernels; nothing here falls back to another path, and
+importing this module fails loudly when the library is not built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libzero.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "zero.h")
+
+ZERO_OK = 0
+ZERO_EINVAL = -1
+ZERO_EALIGN = -2
+ZERO_ERANGE = -3
+ZERO_EDTYPE = -4
+ZERO_ENOMEM = -5
+ZERO_ECUDA = -6
+ZERO_ETIMEOUT = -7
+ZERO_F32 = 0
+ZERO_BF16 = 1
+ZERO_MAX_RANKS = 64
+
+_NAMES = {0: "ZERO_OK", -1: "ZERO_EINVAL", -2: "ZERO_EALIGN", -3: "ZERO_ERANGE",
+          -4: "ZERO_EDTYPE", -5: "ZERO_ENOMEM", -6: "ZERO_ECUDA", -7: "ZERO_ETIMEOUT"}
+
+c_i64 = ctypes.c_int64
+c_i32 = ctypes.c_int32
+c_vp = ctypes.c_void_p
+P = ctypes.POINTER
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, status: int, func: str, cuda_error: int = 0):
+        self.status = status
+        self.name = _NAMES.get(status, str(status))
+        self.cuda_error = cuda_error
+        text = _lib().zero_strerror(status).decode()
+        extra = f" (cudaError {cuda_error})" if status == ZERO_ECUDA else ""
+        super().__init__(f"{func}: {self.name}: {text}{extra}")
+
+
+class zero_plan_info_t(ctypes.Structure):
+    _fields_ = [("psi", c_i64), ("psi_pad", c_i64), ("shard_total", c_i64),
+                ("n_tensors", c_i64), ("n_ranks", c_i32), ("align", c_i32),
+                ("n_groups", c_i32), ("reserved", c_i32)]
+
+
+class zero_group_info_t(ctypes.Structure):
+    _fields_ = [("psi", c_i64), ("psi_pad", c_i64), ("shard", c_i64), ("flat_off", c_i64),
+                ("rank_off", c_i64), ("first_tensor", c_i64), ("n_tensors", c_i64)]
+
+
+class zero_seg_t(ctypes.Structure):
+    _fields_ = [("tensor", c_i64), ("tensor_off", c_i64), ("flat_off", c_i64), ("len", c_i64)]
+
+
+class zero_mem_t(ctypes.Structure):
+    _fields_ = [("values", c_i64), ("bytes", c_i64)]
+
+
+class zero_adam_t(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("grad_scale", ctypes.c_float), ("step", c_i64)]
+
+
+def adam_hp(step: int, grad_scale: float, lr: float = 1e-3, beta1: float = 0.9,
+            beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0) -> zero_adam_t:
+    return zero_adam_t(lr, beta1, beta2, eps, weight_decay, grad_scale, step)
+
+
+_SIGS = {
+    "zero_version": (c_i32, []),
+    "zero_strerror": (ctypes.c_char_p, [c_i32]),
+    "zero_last_cuda_error": (c_i32, []),
+    "zero_plan": (c_i32, [P(c_i64), c_i64, c_i32, c_i32, P(c_i32), P(c_vp)]),
+    "zero_plan_destroy": (c_i32, [c_vp]),
+    "zero_plan_info": (c_i32, [c_vp, P(zero_plan_info_t)]),
+    "zero_plan_group": (c_i32, [c_vp, c_i32, P(zero_group_info_t)]),
+    "zero_plan_tensor": (c_i32, [c_vp, c_i64, P(c_i64), P(c_i32), P(c_i32)]),
+    "zero_plan_shard": (c_i32, [c_vp, c_i32, c_i32, P(c_i64), P(c_i64), P(c_i64)]),
+    "zero_plan_segments": (c_i32, [c_vp, c_i32, P(zero_seg_t), c_i64, P(c_i64)]),
+    "zero_plan_memory": (c_i32, [c_vp, c_i32, P(zero_mem_t)]),
+    "zero_plan_volume": (c_i32, [c_vp, P(c_i64), P(c_i64)]),
+    "zero_rs_partials": (c_i32, [c_vp, c_i32, c_i64, P(c_i64)]),
+    "zero_reduce_scatter": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_i64, c_i64,
+                                    ctypes.c_float, c_vp, c_vp]),
+    "zero_grad_norm": (c_i32, [c_vp, c_i64, ctypes.c_float, c_vp, c_vp, c_vp]),
+    "zero_adam_shard": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, P(zero_adam_t), c_vp,
+                                c_i64, c_i64, c_vp, c_i32, c_vp]),
+    "zero_all_gather": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_i32, c_vp]),
+    "zero_step": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp, P(zero_adam_t), c_vp,
+                          c_vp, c_i32, c_vp]),
+    "zero_step_group": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp,
+                                P(zero_adam_t), c_vp, P(c_vp), c_vp]),
+    "zero_gather_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
+    "zero_layer_checksum": (c_i32, [c_vp, c_i64, c_vp, c_vp]),
+    "zero_copy": (c_i32, [c_vp, c_vp, c_i64, c_vp]),
+}
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/zero.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(zero_\w+)\s*\(", text, re.M)))
+
+
+# -------------------------------------------------------------- marshalling --
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _ptr_array(xs):
+    arr = (c_vp * len(xs))()
+    for i, x in enumerate(xs):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def _check(status: int, func: str) -> None:
+    if status != ZERO_OK:
+        raise ZeroError(status, func, _lib().zero_last_cuda_error() if status == ZERO_ECUDA else 0)
+
+
+class Plan:
+    """Owns a zero_plan_t*; destroyed with the object."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h and _LIB is not None:
+            _LIB.zero_plan_destroy(h)
+
+    @property
+    def _as_parameter_(self):
+        return c_vp(self.handle)
+
+
+# ------------------------------------------------------------ entry points --
+def zero_version() -> int:
+    return _lib().zero_version()
+
+
+def zero_strerror(status: int) -> str:
+    return _lib().zero_strerror(status).decode()
+
+
+def zero_last_cuda_error() -> int:
+    return _lib().zero_last_cuda_error()
+
+
+def zero_plan(numels, n_ranks: int, align: int = 16, group_of_tensor=None) -> Plan:
+    n = len(numels)
+    arr = (c_i64 * max(n, 1))(*[int(v) for v in numels])
+    groups = None
+    if group_of_tensor is not None:
+        groups = (c_i32 * max(n, 1))(*[int(g) for g in group_of_tensor])
+    out = c_vp()
+    _check(_lib().zero_plan(arr, n, n_ranks, align, groups, ctypes.byref(out)), "zero_plan")
+    return Plan(out.value)
+
+
+def zero_plan_destroy(plan: Plan) -> None:
+    """Free the plan now (otherwise it is freed with the Plan object)."""
+    h, plan.handle = plan.handle, None
+    if h:
+        _check(_lib().zero_plan_destroy(h), "zero_plan_destroy")
+
+
+def zero_plan_info(plan: Plan) -> dict:
+    info = zero_plan_info_t()
+    _check(_lib().zero_plan_info(plan, ctypes.byref(info)), "zero_plan_info")
+    return {k: getattr(info, k) for k, _ in info._fields_ if k != "reserved"}
+
+
+def zero_plan_group(plan: Plan, group: int) -> dict:
+    g = zero_group_info_t()
+    _check(_lib().zero_plan_group(plan, group, ctypes.byref(g)), "zero_plan_group")
+    return {k: getattr(g, k) for k, _ in g._fields_}
+
+
+def zero_plan_tensor(plan: Plan, t: int):
+    off, a, b = c_i64(), c_i32(), c_i32()
+    _check(_lib().zero_plan_tensor(plan, t, ctypes.byref(off), ctypes.byref(a), ctypes.byref(b)),
+           "zero_plan_tensor")
+    return off.value, a.value, b.value
+
+
+def zero_plan_shard(plan: Plan, group: int, rank: int):
+    b, n, v = c_i64(), c_i64(), c_i64()
+    _check(_lib().zero_plan_shard(plan, group, rank, ctypes.byref(b), ctypes.byref(n),
+                                  ctypes.byref(v)), "zero_plan_shard")
+    return b.value, n.value, v.value
+
+
+def zero_plan_segments(plan: Plan, rank: int):
+    n = c_i64()
+    _check(_lib().zero_plan_segments(plan, rank, None, 0, ctypes.byref(n)), "zero_plan_segments")
+    buf = (zero_seg_t * max(n.value, 1))()
+    _check(_lib().zero_plan_segments(plan, rank, buf, n.value, ctypes.byref(n)),
+           "zero_plan_segments")
+    return [(s.tensor, s.tensor_off, s.flat_off, s.len) for s in buf[:n.value]]
+
+
+def zero_plan_memory(plan: Plan, stage: int):
+    m = zero_mem_t()
+    _check(_lib().zero_plan_memory(plan, stage, ctypes.byref(m)), "zero_plan_memory")
+    return m.values, m.bytes
+
+
+def zero_plan_volume(plan: Plan):
+    s, r = c_i64(), c_i64()
+    _check(_lib().zero_plan_volume(plan, ctypes.byref(s), ctypes.byref(r)), "zero_plan_volume")
+    return s.value, r.value
+
+
+def zero_rs_partials(plan: Plan, gdtype: int, n_elements: int) -> int:
+    n = c_i64()
+    _check(_lib().zero_rs_partials(plan, gdtype, n_elements, ctypes.byref(n)), "zero_rs_partials")
+    return n.value
+
+
+def zero_reduce_scatter(plan, group, grads, gdtype, reduced, begin, end, grad_scale,
+                        sumsq_partials=None, stream=None) -> None:
+    _check(_lib().zero_reduce_scatter(plan, group, _ptr_array(grads), gdtype, _ptr(reduced),
+                                      begin, end, grad_scale, _ptr(sumsq_partials),
+                                      _stream(stream)), "zero_reduce_scatter")
+
+
+def zero_grad_norm(partials, n, max_norm, d_norm, d_coef, stream=None) -> None:
+    _check(_lib().zero_grad_norm(_ptr(partials), n, max_norm, _ptr(d_norm), _ptr(d_coef),
+                                 _stream(stream)), "zero_grad_norm")
+
+
+def zero_adam_shard(plan, group, master, m, v, reduced, hp, d_coef, begin, end, out,
+                    out_dtype=ZERO_BF16, stream=None) -> None:
+    _check(_lib().zero_adam_shard(plan, group, _ptr(master), _ptr(m), _ptr(v), _ptr(reduced),
+                                  ctypes.byref(hp), _ptr(d_coef), begin, end, _ptr(out),
+                                  out_dtype, _stream(stream)), "zero_adam_shard")
+
+
+def zero_all_gather(plan, group, master, full_out, out_dtype=ZERO_BF16, stream=None) -> None:
+    _check(_lib().zero_all_gather(plan, group, _ptr(master), _ptr(full_out), out_dtype,
+                                  _stream(stream)), "zero_all_gather")
+
+
+def zero_step(plan, group, grads, gdtype, master, m, v, hp, d_coef, full_out,
+              out_dtype=ZERO_BF16, stream=None) -> None:
+    _check(_lib().zero_step(plan, group, _ptr_array(grads), gdtype, _ptr(master), _ptr(m),
+                            _ptr(v), ctypes.byref(hp), _ptr(d_coef), _ptr(full_out), out_dtype,
+                            _stream(stream)), "zero_step")
+
+
+def zero_step_group(plan, group, grads, gdtype, master, m, v, hp, d_coef, shards,
+                    stream=None) -> None:
+    _check(_lib().zero_step_group(plan, group, _ptr_array(grads), gdtype, _ptr(master), _ptr(m),
+                                  _ptr(v), ctypes.byref(hp), _ptr(d_coef), _ptr_array(shards),
+                                  _stream(stream)), "zero_step_group")
+
+
+def zero_gather_layer(plan, group, shards, dtype, layer_out, stream=None) -> None:
+    _check(_lib().zero_gather_layer(plan, group, _ptr_array(shards), dtype, _ptr(layer_out),
+                                    _stream(stream)), "zero_gather_layer")
+
+
+def zero_layer_checksum(layer, n, d_out, stream=None) -> None:
+    _check(_lib().zero_layer_checksum(_ptr(layer), n, _ptr(d_out), _stream(stream)),
+           "zero_layer_checksum")
+
+
+def zero_copy(dst, src, nbytes, stream=None) -> None:
+    _check(_lib().zero_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "zero_copy")

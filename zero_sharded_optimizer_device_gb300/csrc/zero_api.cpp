@@ -1,0 +1,276 @@
+// C-ABI layer of libzero: argument checks, error codes, and the hand-off of
+// plan geometry and Adam constants to the kernels.  No call here allocates
+// device memory.
+#include <math.h>
+#include <stdint.h>
+
+#include "zero_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return ZERO_OK;
+  g_last_cuda = (int)e;
+  return ZERO_ECUDA;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool dtype_ok(int d) { return d == ZERO_F32 || d == ZERO_BF16; }
+
+int check_group(const zero_plan_t* p, int32_t group) {
+  if (!p) return ZERO_EINVAL;
+  if (group < 0 || group >= (int32_t)p->groups.size()) return ZERO_ERANGE;
+  return ZERO_OK;
+}
+
+int check_window(const zero_plan_t* p, int32_t group, int64_t begin, int64_t end) {
+  const zero_group_info_t& g = p->groups[group];
+  if (begin < 0 || end < begin || end > g.psi_pad) return ZERO_ERANGE;
+  return ZERO_OK;
+}
+
+// A host array of N device pointers, each non-null and 16-byte aligned.
+template <typename P>
+int check_rank_ptrs(const zero_plan_t* p, P const* ptrs) {
+  if (!ptrs) return ZERO_EINVAL;
+  for (int r = 0; r < p->n_ranks; ++r) {
+    if (!ptrs[r]) return ZERO_EINVAL;
+    if (!aligned16(ptrs[r])) return ZERO_EALIGN;
+  }
+  return ZERO_OK;
+}
+
+int check_buf(const void* q) {
+  if (!q) return ZERO_EINVAL;
+  return aligned16(q) ? ZERO_OK : ZERO_EALIGN;
+}
+
+int check_opt_buf(const void* q) { return (!q || aligned16(q)) ? ZERO_OK : ZERO_EALIGN; }
+
+// fp32 scalars (norm, clip coefficient) are read and written singly.
+int check_opt_f32(const void* q) { return (!q || ((uintptr_t)q & 3u) == 0) ? ZERO_OK : ZERO_EALIGN; }
+
+// fp64 partial sums are read and written one value at a time.
+int check_opt_f64(const void* q) { return (!q || ((uintptr_t)q & 7u) == 0) ? ZERO_OK : ZERO_EALIGN; }
+
+zk::GroupK group_k(const zero_plan_t* p, int32_t group) {
+  const zero_group_info_t& g = p->groups[group];
+  zk::GroupK k;
+  k.S = g.shard;
+  k.flat_off = g.flat_off;
+  k.rank_off = g.rank_off;
+  k.invS = g.shard > 0 ? 1.0f / (float)g.shard : 0.0f;
+  k.n = p->n_ranks;
+  return k;
+}
+
+zk::RankPtrs rank_ptrs(const zero_plan_t* p, const void* const* ptrs) {
+  zk::RankPtrs r{};
+  for (int i = 0; i < p->n_ranks; ++i) r.p[i] = ptrs[i];
+  return r;
+}
+
+// Adam constants.  The bias corrections 1 - beta^t: beta (fp32) raised to t
+// by t successive fp64 multiplications (stopping once beta^t < 2^-60, when
+// 1 - beta^t is exactly 1 in fp64), subtracted from 1 in fp64, rounded once
+// to fp32.  (1 - beta) and lr*wd are fp32 operations.
+int adam_k(const zero_adam_t* hp, zk::AdamK* out) {
+  if (!hp) return ZERO_EINVAL;
+  if (hp->step < 1) return ZERO_EINVAL;
+  if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+    return ZERO_EINVAL;
+  if (!isfinite(hp->lr) || !isfinite(hp->eps) || !isfinite(hp->weight_decay) ||
+      !isfinite(hp->grad_scale))
+    return ZERO_EINVAL;
+  double p1 = 1.0, p2 = 1.0;
+  const double b1 = (double)hp->beta1, b2 = (double)hp->beta2;
+  const double tiny = 8.673617379884035e-19;  // 2^-60
+  for (int64_t t = 0; t < hp->step && (p1 >= tiny || p2 >= tiny); ++t) {
+    if (p1 >= tiny) p1 *= b1;
+    if (p2 >= tiny) p2 *= b2;
+  }
+  zk::AdamK k;
+  k.lr = hp->lr;
+  k.b1 = hp->beta1;
+  k.b2 = hp->beta2;
+  k.omb1 = 1.0f - hp->beta1;
+  k.omb2 = 1.0f - hp->beta2;
+  k.eps = hp->eps;
+  k.bc1 = (float)(1.0 - p1);
+  k.bc2 = (float)(1.0 - p2);
+  k.lrwd = hp->lr * hp->weight_decay;
+  k.has_wd = hp->weight_decay != 0.0f;
+  k.scale = hp->grad_scale;
+  *out = k;
+  return ZERO_OK;
+}
+
+#define ZERO_TRY(x)              \
+  do {                           \
+    int _s = (x);                \
+    if (_s != ZERO_OK) return _s; \
+  } while (0)
+
+}  // namespace
+
+extern "C" int zero_version(void) { return 10000; }
+
+extern "C" const char* zero_strerror(int status) {
+  switch (status) {
+    case ZERO_OK: return "ok";
+    case ZERO_EINVAL: return "invalid argument";
+    case ZERO_EALIGN: return "device pointer not 16-byte aligned";
+    case ZERO_ERANGE: return "group, rank, tensor or window outside the plan";
+    case ZERO_EDTYPE: return "unsupported dtype";
+    case ZERO_ENOMEM: return "host allocation failed";
+    case ZERO_ECUDA: return "CUDA runtime error";
+    case ZERO_ETIMEOUT: return "bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int zero_last_cuda_error(void) { return g_last_cuda; }
+
+extern "C" int zero_rs_partials(const zero_plan_t* plan, zero_dtype_t gdtype, int64_t n_elements,
+                                int64_t* n_partials) {
+  if (!plan || !n_partials || n_elements < 0) return ZERO_EINVAL;
+  if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
+  *n_partials = zk::rs_partials_for(plan->n_ranks, gdtype, n_elements);
+  return ZERO_OK;
+}
+
+extern "C" int zero_reduce_scatter(const zero_plan_t* plan, int32_t group,
+                                   const void* const* grads, zero_dtype_t gdtype, float* reduced,
+                                   int64_t begin, int64_t end, float grad_scale,
+                                   double* sumsq_partials, zero_stream_t stream) {
+  ZERO_TRY(check_group(plan, group));
+  if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_window(plan, group, begin, end));
+  ZERO_TRY(check_rank_ptrs(plan, grads));
+  ZERO_TRY(check_buf(reduced));
+  ZERO_TRY(check_opt_f64(sumsq_partials));
+  return cuda_status(zk::launch_reduce_scatter(rank_ptrs(plan, grads), gdtype,
+                                               group_k(plan, group), reduced, begin, end,
+                                               grad_scale, sumsq_partials,
+                                               (cudaStream_t)stream));
+}
+
+extern "C" int zero_grad_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
+                              float* d_coef, zero_stream_t stream) {
+  if (n < 0 || (n > 0 && !partials) || !isfinite(max_norm) || max_norm <= 0.0f)
+    return ZERO_EINVAL;
+  ZERO_TRY(check_opt_f64(partials));
+  ZERO_TRY(check_opt_f32(d_norm));
+  ZERO_TRY(check_opt_f32(d_coef));
+  return cuda_status(zk::launch_norm(partials, n, max_norm, d_norm, d_coef, (cudaStream_t)stream));
+}
+
+extern "C" int zero_adam_shard(const zero_plan_t* plan, int32_t group, float* master, float* m,
+                               float* v, const float* reduced, const zero_adam_t* hp,
+                               const float* d_coef, int64_t begin, int64_t end, void* out,
+                               zero_dtype_t out_dtype, zero_stream_t stream) {
+  ZERO_TRY(check_group(plan, group));
+  ZERO_TRY(check_window(plan, group, begin, end));
+  ZERO_TRY(check_buf(master));
+  ZERO_TRY(check_buf(m));
+  ZERO_TRY(check_buf(v));
+  ZERO_TRY(check_buf(reduced));
+  ZERO_TRY(check_opt_buf(out));
+  if (out && !dtype_ok(out_dtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_opt_f32(d_coef));
+  zk::AdamK k;
+  ZERO_TRY(adam_k(hp, &k));
+  const int mode = !out ? zk::OUT_NONE
+                        : (out_dtype == ZERO_BF16 ? zk::OUT_FULL_BF16 : zk::OUT_FULL_F32);
+  return cuda_status(zk::launch_adam(group_k(plan, group), begin, end, master, m, v, reduced, k,
+                                     d_coef, mode, out, (cudaStream_t)stream));
+}
+
+extern "C" int zero_all_gather(const zero_plan_t* plan, int32_t group, const float* master,
+                               void* full_out, zero_dtype_t out_dtype, zero_stream_t stream) {
+  if (!plan) return ZERO_EINVAL;
+  if (group != -1) ZERO_TRY(check_group(plan, group));
+  if (!dtype_ok(out_dtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_buf(master));
+  ZERO_TRY(check_buf(full_out));
+  int64_t a = 0, b = plan->psi_pad;
+  if (group >= 0) {
+    a = plan->groups[group].flat_off;
+    b = a + plan->groups[group].psi_pad;
+  }
+  return cuda_status(zk::launch_cast(master, a, b, out_dtype, full_out, (cudaStream_t)stream));
+}
+
+extern "C" int zero_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                         zero_dtype_t gdtype, float* master, float* m, float* v,
+                         const zero_adam_t* hp, const float* d_coef, void* full_out,
+                         zero_dtype_t out_dtype, zero_stream_t stream) {
+  ZERO_TRY(check_group(plan, group));
+  if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_rank_ptrs(plan, grads));
+  ZERO_TRY(check_buf(master));
+  ZERO_TRY(check_buf(m));
+  ZERO_TRY(check_buf(v));
+  ZERO_TRY(check_opt_buf(full_out));
+  if (full_out && !dtype_ok(out_dtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_opt_f32(d_coef));
+  zk::AdamK k;
+  ZERO_TRY(adam_k(hp, &k));
+  const int mode = !full_out ? zk::OUT_NONE
+                             : (out_dtype == ZERO_BF16 ? zk::OUT_FULL_BF16 : zk::OUT_FULL_F32);
+  zk::OutPtrs none{};
+  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), gdtype, group_k(plan, group), 0,
+                                      plan->groups[group].psi_pad, master, m, v, k, d_coef, mode,
+                                      full_out, none, (cudaStream_t)stream));
+}
+
+extern "C" int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                               zero_dtype_t gdtype, float* master, float* m, float* v,
+                               const zero_adam_t* hp, const float* d_coef, void* const* shards,
+                               zero_stream_t stream) {
+  ZERO_TRY(check_group(plan, group));
+  if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_rank_ptrs(plan, grads));
+  ZERO_TRY(check_rank_ptrs(plan, shards));
+  ZERO_TRY(check_buf(master));
+  ZERO_TRY(check_buf(m));
+  ZERO_TRY(check_buf(v));
+  ZERO_TRY(check_opt_f32(d_coef));
+  zk::AdamK k;
+  ZERO_TRY(adam_k(hp, &k));
+  zk::OutPtrs out{};
+  for (int r = 0; r < plan->n_ranks; ++r) out.p[r] = shards[r];
+  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), gdtype, group_k(plan, group), 0,
+                                      plan->groups[group].psi_pad, master, m, v, k, d_coef,
+                                      zk::OUT_SHARDS_BF16, nullptr, out, (cudaStream_t)stream));
+}
+
+extern "C" int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
+                                 zero_dtype_t dtype, void* layer_out, zero_stream_t stream) {
+  ZERO_TRY(check_group(plan, group));
+  if (!dtype_ok(dtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_rank_ptrs(plan, shards));
+  ZERO_TRY(check_buf(layer_out));
+  return cuda_status(zk::launch_gather(rank_ptrs(plan, shards), dtype == ZERO_BF16 ? 2 : 4,
+                                       group_k(plan, group), plan->groups[group].psi_pad,
+                                       layer_out, (cudaStream_t)stream));
+}
+
+extern "C" int zero_layer_checksum(const void* layer, int64_t n, uint64_t* d_out,
+                                   zero_stream_t stream) {
+  if (n < 0 || !d_out || (n > 0 && !layer)) return ZERO_EINVAL;
+  ZERO_TRY(check_opt_buf(layer));
+  if (((uintptr_t)d_out & 7u) != 0) return ZERO_EALIGN;
+  return cuda_status(zk::launch_checksum(layer, n, d_out, (cudaStream_t)stream));
+}
+
+extern "C" int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_t stream) {
+  if (bytes < 0 || (bytes % 16) != 0) return ZERO_EINVAL;
+  if (bytes == 0) return ZERO_OK;
+  ZERO_TRY(check_buf(dst));
+  ZERO_TRY(check_buf(src));
+  return cuda_status(zk::launch_copy(dst, src, bytes, (cudaStream_t)stream));
+}

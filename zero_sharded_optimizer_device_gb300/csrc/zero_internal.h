@@ -1,0 +1,83 @@
+// Private declarations shared by the planner, the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "zero.h"
+
+// Opaque plan (see zero_plan in zero.h).
+struct zero_plan {
+  int32_t n_ranks = 0;
+  int32_t align = 0;
+  std::vector<int64_t> numels;
+  std::vector<int32_t> tensor_group;
+  std::vector<int64_t> tensor_group_off;  // offset of the tensor inside its group
+  std::vector<zero_group_info_t> groups;
+  int64_t psi = 0, psi_pad = 0, shard_total = 0;
+};
+
+namespace zk {
+
+constexpr int kMaxRanks = ZERO_MAX_RANKS;
+
+// N rank pointers, passed to kernels by value (kernel parameter space).
+struct RankPtrs {
+  const void* p[kMaxRanks];
+};
+struct OutPtrs {
+  void* p[kMaxRanks];
+};
+
+// One group's geometry as the kernels see it.
+struct GroupK {
+  int64_t S;         // shard size
+  int64_t flat_off;  // group start in flat arrays
+  int64_t rank_off;  // group start in per-rank shard buffers
+  float invS;        // ~1/S, refined with integer checks
+  int n;             // ranks
+};
+
+// Adam constants prepared on the host (fp32 values; bc from fp64).
+struct AdamK {
+  float lr, b1, b2, omb1, omb2, eps, bc1, bc2, lrwd, scale;
+  int has_wd;
+};
+
+enum OutMode : int { OUT_NONE = 0, OUT_FULL_BF16 = 1, OUT_FULL_F32 = 2, OUT_SHARDS_BF16 = 3 };
+
+// Launchers (zero_kernels.cu, zero_rs.cu).  Each returns the launch status.
+cudaError_t launch_reduce_scatter(const RankPtrs& src, int gdtype, const GroupK& g,
+                                  float* reduced, int64_t begin, int64_t end, float scale,
+                                  double* partials, cudaStream_t st);
+int64_t rs_partials_for(int n, int gdtype, int64_t n_elements);
+
+cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64_t begin,
+                         int64_t end, float* master, float* m, float* v, const AdamK& h,
+                         const float* coef, int out_mode, void* out_full,
+                         const OutPtrs& shards, cudaStream_t st);
+
+cudaError_t launch_adam(const GroupK& g, int64_t begin, int64_t end, float* master, float* m,
+                        float* v, const float* reduced, const AdamK& h, const float* coef,
+                        int out_mode, void* out, cudaStream_t st);
+
+// dst[i] = cast(src[i]) for flat indices i in [a, b).
+cudaError_t launch_cast(const float* src, int64_t a, int64_t b, int out_dtype, void* dst,
+                        cudaStream_t st);
+
+cudaError_t launch_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
+                        float* d_coef, cudaStream_t st);
+
+cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
+                          int64_t psi_pad, void* out, cudaStream_t st);
+
+cudaError_t launch_checksum(const void* layer, int64_t n, uint64_t* out, cudaStream_t st);
+
+cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t st);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace zk

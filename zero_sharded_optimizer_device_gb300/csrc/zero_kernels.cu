@@ -1,0 +1,283 @@
+// Unfused pieces of the step and the stage-3 gather:
+//   adam_kernel     Adam over a window of the materialised reduced gradient
+//   cast_kernel     all-gather of the updated parameters into the full buffer
+//   norm_kernel     global gradient norm and clip coefficient
+//   gather_kernel   stage-3 per-layer gather of N rank shards
+//   checksum_kernel consumer of a gathered layer
+//   copy_kernel     16-byte device copy (achievable HBM bandwidth)
+#include <mutex>
+#include <unordered_map>
+
+#include "zero_device.cuh"
+
+namespace zk {
+
+namespace {
+
+template <typename K>
+int64_t wave_grid(K kernel, int64_t items) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> cache[16];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int nb = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto& c = cache[dev & 15];
+    auto it = c.find(reinterpret_cast<const void*>(kernel));
+    if (it != c.end()) {
+      nb = it->second;
+    } else {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess ||
+          nb < 1)
+        nb = 1;
+      c[reinterpret_cast<const void*>(kernel)] = nb;
+    }
+  }
+  int64_t want = (items + kThreads - 1) / kThreads;
+  const int64_t cap = (int64_t)sm_count() * nb;
+  if (want > cap) want = cap;
+  return want < 1 ? 1 : want;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Adam on [begin, end) of a group from the fp32 reduced gradient.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+    adam_kernel(GroupK g, int64_t begin, int64_t end, float* __restrict__ master,
+                float* __restrict__ mom, float* __restrict__ var,
+                const float* __restrict__ reduced, AdamK h, const float* __restrict__ coef_ptr,
+                int out_mode, void* __restrict__ out) {
+  const float coef = coef_ptr ? *coef_ptr : 1.0f;
+  const int64_t q0 = begin >> 3, q1 = (end + 7) >> 3;
+  const bool flat_vec_ok = (g.flat_off & 7) == 0;
+  for (int64_t q = q0 + gtid(); q < q1; q += gstride()) {
+    const int64_t i = q << 3;
+    const int64_t f = g.flat_off + i;
+    if (flat_vec_ok && i >= begin && i + 8 <= end) {
+      const uint4 r0 = ld_once(reduced + f), r1 = ld_once(reduced + f + 4);
+      const float4 p0 = ld_state(master + f), p1 = ld_state(master + f + 4);
+      const float4 m0 = ld_state(mom + f), m1 = ld_state(mom + f + 4);
+      const float4 v0 = ld_state(var + f), v1 = ld_state(var + f + 4);
+      float r[8] = {__uint_as_float(r0.x), __uint_as_float(r0.y), __uint_as_float(r0.z),
+                    __uint_as_float(r0.w), __uint_as_float(r1.x), __uint_as_float(r1.y),
+                    __uint_as_float(r1.z), __uint_as_float(r1.w)};
+      float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) adam1(p[e], m[e], v[e], scaled(r[e], h, coef), h);
+      st_stream(master + f, make_float4(p[0], p[1], p[2], p[3]));
+      st_stream(master + f + 4, make_float4(p[4], p[5], p[6], p[7]));
+      st_stream(mom + f, make_float4(m[0], m[1], m[2], m[3]));
+      st_stream(mom + f + 4, make_float4(m[4], m[5], m[6], m[7]));
+      st_stream(var + f, make_float4(v[0], v[1], v[2], v[3]));
+      st_stream(var + f + 4, make_float4(v[4], v[5], v[6], v[7]));
+      if (out_mode == OUT_FULL_BF16) {
+        st_stream(static_cast<uint16_t*>(out) + f,
+                  make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                             pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7])));
+      } else if (out_mode == OUT_FULL_F32) {
+        float* o = static_cast<float*>(out) + f;
+        st_stream(o, make_float4(p[0], p[1], p[2], p[3]));
+        st_stream(o + 4, make_float4(p[4], p[5], p[6], p[7]));
+      }
+    } else {
+      for (int e = 0; e < 8; ++e) {
+        const int64_t j = i + e;
+        if (j < begin || j >= end) continue;
+        float p = master[f + e], m = mom[f + e], v = var[f + e];
+        adam1(p, m, v, scaled(reduced[f + e], h, coef), h);
+        master[f + e] = p;
+        mom[f + e] = m;
+        var[f + e] = v;
+        if (out_mode == OUT_FULL_BF16) static_cast<uint16_t*>(out)[f + e] = to_bf16(p);
+        else if (out_mode == OUT_FULL_F32) static_cast<float*>(out)[f + e] = p;
+      }
+    }
+  }
+}
+
+cudaError_t launch_adam(const GroupK& g, int64_t begin, int64_t end, float* master, float* m,
+                        float* v, const float* reduced, const AdamK& h, const float* coef,
+                        int out_mode, void* out, cudaStream_t st) {
+  if (end <= begin) return cudaSuccess;
+  const int64_t vecs = ((end + 7) >> 3) - (begin >> 3);
+  adam_kernel<<<(unsigned)wave_grid(adam_kernel, vecs), kThreads, 0, st>>>(
+      g, begin, end, master, m, v, reduced, h, coef, out_mode, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// All-gather: dst[i] = cast(src[i]) for i in [a, b) (flat indices).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+    cast_kernel(const float* __restrict__ src, int64_t a, int64_t b, int out_dtype,
+                void* __restrict__ dst) {
+  const int64_t q0 = a >> 3, q1 = (b + 7) >> 3;
+  for (int64_t q = q0 + gtid(); q < q1; q += gstride()) {
+    const int64_t i = q << 3;
+    if (i >= a && i + 8 <= b) {
+      const uint4 x0 = ld_once(src + i), x1 = ld_once(src + i + 4);
+      if (out_dtype == ZERO_BF16) {
+        st_stream(static_cast<uint16_t*>(dst) + i,
+                  make_uint4(pack_bf16x2(__uint_as_float(x0.x), __uint_as_float(x0.y)),
+                             pack_bf16x2(__uint_as_float(x0.z), __uint_as_float(x0.w)),
+                             pack_bf16x2(__uint_as_float(x1.x), __uint_as_float(x1.y)),
+                             pack_bf16x2(__uint_as_float(x1.z), __uint_as_float(x1.w))));
+      } else {
+        float* o = static_cast<float*>(dst) + i;
+        st_stream((void*)o, x0);
+        st_stream((void*)(o + 4), x1);
+      }
+    } else {
+      for (int e = 0; e < 8; ++e) {
+        const int64_t j = i + e;
+        if (j < a || j >= b) continue;
+        if (out_dtype == ZERO_BF16) static_cast<uint16_t*>(dst)[j] = to_bf16(src[j]);
+        else static_cast<float*>(dst)[j] = src[j];
+      }
+    }
+  }
+}
+
+cudaError_t launch_cast(const float* src, int64_t a, int64_t b, int out_dtype, void* dst,
+                        cudaStream_t st) {
+  if (b <= a) return cudaSuccess;
+  const int64_t vecs = ((b + 7) >> 3) - (a >> 3);
+  cast_kernel<<<(unsigned)wave_grid(cast_kernel, vecs), kThreads, 0, st>>>(src, a, b, out_dtype,
+                                                                           dst);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Global norm: one block sums the fp64 partials in a fixed order.
+// ---------------------------------------------------------------------------
+constexpr int kNormThreads = 1024;
+
+__global__ void __launch_bounds__(kNormThreads)
+    norm_kernel(const double* __restrict__ partials, int64_t n, float max_norm,
+                float* __restrict__ d_norm, float* __restrict__ d_coef) {
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < n; i += kNormThreads) s += partials[i];
+  __shared__ double red[kNormThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    double t = red[threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
+    if (threadIdx.x == 0) {
+      const double norm = sqrt(t);
+      double coef = (double)max_norm / (norm + 1e-6);
+      if (coef > 1.0) coef = 1.0;
+      if (d_norm) *d_norm = (float)norm;
+      if (d_coef) *d_coef = (float)coef;
+    }
+  }
+}
+
+cudaError_t launch_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
+                        float* d_coef, cudaStream_t st) {
+  norm_kernel<<<1, kNormThreads, 0, st>>>(partials, n, max_norm, d_norm, d_coef);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Stage-3 gather: out[j] = shards[j / S][rank_off + j % S], j < psi_pad.
+// ---------------------------------------------------------------------------
+template <int ES>
+__global__ void __launch_bounds__(kThreads)
+    gather_kernel(RankPtrs shards, GroupK g, int64_t psi_pad, void* __restrict__ out) {
+  constexpr int VW = 16 / ES;  // elements per 16-byte vector
+  const bool vec_ok = ((g.S | g.rank_off) % VW) == 0;
+  if (vec_ok) {
+    const int64_t nv = psi_pad / VW;  // psi_pad is a multiple of S, so of VW
+    for (int64_t q = gtid(); q < nv; q += gstride()) {
+      const int64_t j = q * VW;
+      const int k = owner_of(j, g);
+      const char* s = static_cast<const char*>(shards.p[k]) +
+                      (g.rank_off + (j - (int64_t)k * g.S)) * ES;
+      st_stream(static_cast<char*>(out) + j * ES, ld_once(s));
+    }
+  } else {
+    for (int64_t j = gtid(); j < psi_pad; j += gstride()) {
+      const int k = owner_of(j, g);
+      const int64_t src = g.rank_off + (j - (int64_t)k * g.S);
+      if (ES == 2)
+        static_cast<uint16_t*>(out)[j] = static_cast<const uint16_t*>(shards.p[k])[src];
+      else
+        static_cast<uint32_t*>(out)[j] = static_cast<const uint32_t*>(shards.p[k])[src];
+    }
+  }
+}
+
+cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
+                          int64_t psi_pad, void* out, cudaStream_t st) {
+  if (psi_pad <= 0) return cudaSuccess;
+  if (elem_bytes == 2) {
+    gather_kernel<2><<<(unsigned)wave_grid(gather_kernel<2>, psi_pad / 8 + 1), kThreads, 0, st>>>(
+        shards, g, psi_pad, out);
+  } else {
+    gather_kernel<4><<<(unsigned)wave_grid(gather_kernel<4>, psi_pad / 4 + 1), kThreads, 0, st>>>(
+        shards, g, psi_pad, out);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Layer consumer: sum of bits[j] * (1 + (j mod 65536)), mod 2^64.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+    checksum_kernel(const uint16_t* __restrict__ bits, int64_t n,
+                    unsigned long long* __restrict__ out) {
+  unsigned long long s = 0;
+  const int64_t nv = n >> 3;
+  for (int64_t q = gtid(); q < nv; q += gstride()) {
+    const uint4 x = ld_once(bits + q * 8);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    const int64_t j0 = q * 8;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t j = j0 + 2 * e;
+      s += (unsigned long long)(w[e] & 0xFFFFu) * (1ull + (unsigned long long)(j & 0xFFFF));
+      s += (unsigned long long)(w[e] >> 16) * (1ull + (unsigned long long)((j + 1) & 0xFFFF));
+    }
+  }
+  for (int64_t j = (nv << 3) + gtid(); j < n; j += gstride())
+    s += (unsigned long long)bits[j] * (1ull + (unsigned long long)(j & 0xFFFF));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0 && s != 0) atomicAdd(out, s);
+}
+
+cudaError_t launch_checksum(const void* layer, int64_t n, uint64_t* out, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(uint64_t), st);
+  if (e != cudaSuccess) return e;
+  if (n <= 0) return cudaSuccess;
+  checksum_kernel<<<(unsigned)wave_grid(checksum_kernel, n / 8 + 1), kThreads, 0, st>>>(
+      static_cast<const uint16_t*>(layer), n, reinterpret_cast<unsigned long long*>(out));
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Copy (bytes a multiple of 16).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+    copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t nv) {
+  for (int64_t q = gtid(); q < nv; q += gstride()) st_stream(dst + q, ld_once(src + q));
+}
+
+cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t st) {
+  const int64_t nv = bytes / 16;
+  if (nv <= 0) return cudaSuccess;
+  copy_kernel<<<(unsigned)wave_grid(copy_kernel, nv), kThreads, 0, st>>>(
+      static_cast<uint4*>(dst), static_cast<const uint4*>(src), nv);
+  return cudaGetLastError();
+}
+
+}  // namespace zk

@@ -1,0 +1,292 @@
+// Reduce-scatter over N emulated ranks, and the fused reduce-scatter + scale
+// + Adam + all-gather step.
+//
+// ["[REQUEST] Direct Correspondence between Gradient and Optimizer States to
+// Reduce Communication?", "Problem"]: reduce-scatter the gradients to the
+// owners of the optimizer state, update, all-gather the parameters.  All N
+// ranks live on this GPU as N gradient buffers, so the reduce-scatter is an
+// on-chip N-source reduction in the ring order (zero_device.cuh) and the
+// all-gather is the write of the updated parameters into the one full flat
+// parameter buffer (or, stage 3, into each owner's shard buffer).
+//
+// Both kernels stream: every thread owns 8 consecutive elements per
+// iteration, loads them from the N sources with 16-byte loads, and the grid
+// strides over the window with one resident wave of blocks.
+#include <mutex>
+#include <unordered_map>
+
+#include "zero_device.cuh"
+
+namespace zk {
+
+namespace {
+
+// Resident blocks per SM for a kernel (cached per kernel and device).
+template <typename K>
+int resident_blocks(K kernel, int threads) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> cache[16];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const void* key = reinterpret_cast<const void*>(kernel);
+  std::lock_guard<std::mutex> lock(mu);
+  auto& c = cache[dev & 15];
+  auto it = c.find(key);
+  if (it != c.end()) return it->second;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess ||
+      nb < 1)
+    nb = 1;
+  c[key] = nb;
+  return nb;
+}
+
+int64_t grid_for(int64_t items, int threads, int per_sm) {
+  int64_t want = (items + threads - 1) / threads;
+  int64_t cap = (int64_t)sm_count() * per_sm;
+  if (want > cap) want = cap;
+  return want < 1 ? 1 : want;
+}
+
+}  // namespace
+
+int sm_count() {
+  static int cached[16] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int& c = cached[dev & 15];
+  if (c == 0) {
+    int s = 0;
+    cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev);
+    c = s > 0 ? s : 1;
+  }
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// Reduce-scatter: reduced[flat_off + i] = ring sum, i in [begin, end);
+// optional fp64 per-block partial sums of (reduced*scale)^2.
+// ---------------------------------------------------------------------------
+template <int NT, typename GT>
+__global__ void __launch_bounds__(kThreads)
+    rs_kernel(RankPtrs src, GroupK g, int64_t begin, int64_t end, float* __restrict__ reduced,
+              float scale, double* __restrict__ partials) {
+  const int n = NT > 0 ? NT : g.n;
+  const int64_t q0 = begin >> 3, q1 = (end + 7) >> 3;
+  const bool flat_vec_ok = (g.flat_off & 7) == 0;  // 16-byte vectors in flat arrays
+  double ss = 0.0;
+  for (int64_t q = q0 + gtid(); q < q1; q += gstride()) {
+    const int64_t i = q << 3;
+    const int k = owner_of(i, g);
+    float* out = reduced + g.flat_off + i;
+    if (flat_vec_ok && i >= begin && i + 8 <= end && i + 7 < (int64_t)(k + 1) * g.S) {
+      float acc[8];
+      ring_sum8<NT, GT>(src, n, k, i, acc);
+      st_stream(out, make_float4(acc[0], acc[1], acc[2], acc[3]));
+      st_stream(out + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+      if (partials) {
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = __fmul_rn(acc[e], scale);
+          s = __fadd_rn(s, __fmul_rn(x, x));
+        }
+        ss += (double)s;
+      }
+    } else {
+      float s = 0.f;
+      for (int e = 0; e < 8; ++e) {
+        const int64_t j = i + e;
+        if (j < begin || j >= end) continue;
+        const float r = ring_sum1<GT>(src, n, owner_of(j, g), j);
+        out[e] = r;
+        const float x = __fmul_rn(r, scale);
+        s = __fadd_rn(s, __fmul_rn(x, x));
+      }
+      ss += (double)s;
+    }
+  }
+  if (!partials) return;
+  // fixed-order block reduction: warp shuffle tree, then warp 0
+  __shared__ double red[kThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_down_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    double t = threadIdx.x < kThreads / 32 ? red[threadIdx.x] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
+    if (threadIdx.x == 0) partials[blockIdx.x] = t;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Fused step: ring sum -> scale (-> clip) -> Adam -> cast, one pass.
+// ---------------------------------------------------------------------------
+template <int NT, typename GT>
+__global__ void __launch_bounds__(kThreads)
+    fused_kernel(RankPtrs src, GroupK g, int64_t begin, int64_t end, float* __restrict__ master,
+                 float* __restrict__ mom, float* __restrict__ var, AdamK h,
+                 const float* __restrict__ coef_ptr, int out_mode, void* __restrict__ out_full,
+                 OutPtrs shards) {
+  const int n = NT > 0 ? NT : g.n;
+  const float coef = coef_ptr ? *coef_ptr : 1.0f;
+  const int64_t q0 = begin >> 3, q1 = (end + 7) >> 3;
+  const bool shard_vec_ok = ((g.rank_off | g.S) & 7) == 0;
+  const bool flat_vec_ok = (g.flat_off & 7) == 0;  // 16-byte vectors in flat arrays
+  for (int64_t q = q0 + gtid(); q < q1; q += gstride()) {
+    const int64_t i = q << 3;
+    const int64_t f = g.flat_off + i;
+    const int k = owner_of(i, g);
+    if (flat_vec_ok && i >= begin && i + 8 <= end && i + 7 < (int64_t)(k + 1) * g.S) {
+      const float4 p0 = ld_state(master + f), p1 = ld_state(master + f + 4);
+      const float4 m0 = ld_state(mom + f), m1 = ld_state(mom + f + 4);
+      const float4 v0 = ld_state(var + f), v1 = ld_state(var + f + 4);
+      float acc[8];
+      ring_sum8<NT, GT>(src, n, k, i, acc);
+      float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) adam1(p[e], m[e], v[e], scaled(acc[e], h, coef), h);
+      st_stream(master + f, make_float4(p[0], p[1], p[2], p[3]));
+      st_stream(master + f + 4, make_float4(p[4], p[5], p[6], p[7]));
+      st_stream(mom + f, make_float4(m[0], m[1], m[2], m[3]));
+      st_stream(mom + f + 4, make_float4(m[4], m[5], m[6], m[7]));
+      st_stream(var + f, make_float4(v[0], v[1], v[2], v[3]));
+      st_stream(var + f + 4, make_float4(v[4], v[5], v[6], v[7]));
+      if (out_mode == OUT_FULL_BF16) {
+        st_stream(static_cast<uint16_t*>(out_full) + f,
+                  make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                             pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7])));
+      } else if (out_mode == OUT_FULL_F32) {
+        float* o = static_cast<float*>(out_full) + f;
+        st_stream(o, make_float4(p[0], p[1], p[2], p[3]));
+        st_stream(o + 4, make_float4(p[4], p[5], p[6], p[7]));
+      } else if (out_mode == OUT_SHARDS_BF16) {
+        uint16_t* o = static_cast<uint16_t*>(shards.p[k]) + g.rank_off + (i - (int64_t)k * g.S);
+        if (shard_vec_ok) {
+          st_stream(o, make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                                  pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7])));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = to_bf16(p[e]);
+        }
+      }
+    } else {
+      for (int e = 0; e < 8; ++e) {
+        const int64_t j = i + e;
+        if (j < begin || j >= end) continue;
+        const int kj = owner_of(j, g);
+        const float r = ring_sum1<GT>(src, n, kj, j);
+        float p = master[f + e], m = mom[f + e], v = var[f + e];
+        adam1(p, m, v, scaled(r, h, coef), h);
+        master[f + e] = p;
+        mom[f + e] = m;
+        var[f + e] = v;
+        if (out_mode == OUT_FULL_BF16) {
+          static_cast<uint16_t*>(out_full)[f + e] = to_bf16(p);
+        } else if (out_mode == OUT_FULL_F32) {
+          static_cast<float*>(out_full)[f + e] = p;
+        } else if (out_mode == OUT_SHARDS_BF16) {
+          static_cast<uint16_t*>(shards.p[kj])[g.rank_off + (j - (int64_t)kj * g.S)] = to_bf16(p);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch on N (compile-time specialisations for common N) and dtype.
+// ---------------------------------------------------------------------------
+namespace {
+
+template <template <int, typename> class Launch, typename... A>
+cudaError_t dispatch(int n, int gdtype, A&&... a) {
+  if (gdtype == ZERO_BF16) {
+    switch (n) {
+      case 2: return Launch<2, uint16_t>::run(a...);
+      case 4: return Launch<4, uint16_t>::run(a...);
+      case 8: return Launch<8, uint16_t>::run(a...);
+      case 16: return Launch<16, uint16_t>::run(a...);
+      case 32: return Launch<32, uint16_t>::run(a...);
+      case 64: return Launch<64, uint16_t>::run(a...);
+      default: return Launch<0, uint16_t>::run(a...);
+    }
+  }
+  switch (n) {
+    case 2: return Launch<2, float>::run(a...);
+    case 4: return Launch<4, float>::run(a...);
+    case 8: return Launch<8, float>::run(a...);
+    case 16: return Launch<16, float>::run(a...);
+    case 32: return Launch<32, float>::run(a...);
+    case 64: return Launch<64, float>::run(a...);
+    default: return Launch<0, float>::run(a...);
+  }
+}
+
+template <int NT, typename GT>
+struct RsLaunch {
+  // One grid for a window of n elements: one block per 256 vectors, at most
+  // one resident wave.  The partial count a caller reserves is this grid.
+  static int64_t grid(int64_t n_elements) {
+    const int64_t vecs = (n_elements + 7) / 8 + 1;
+    return grid_for(vecs, kThreads, resident_blocks(rs_kernel<NT, GT>, kThreads));
+  }
+  static cudaError_t run(const RankPtrs& src, const GroupK& g, int64_t begin, int64_t end,
+                         float* reduced, float scale, double* partials, cudaStream_t st) {
+    rs_kernel<NT, GT><<<(unsigned)grid(end - begin), kThreads, 0, st>>>(src, g, begin, end,
+                                                                        reduced, scale, partials);
+    return cudaGetLastError();
+  }
+};
+
+template <int NT, typename GT>
+struct RsGrid {
+  static cudaError_t run(int64_t n_elements, int64_t* out) {
+    *out = RsLaunch<NT, GT>::grid(n_elements);
+    return cudaSuccess;
+  }
+};
+
+template <int NT, typename GT>
+struct FusedLaunch {
+  static cudaError_t run(const RankPtrs& src, const GroupK& g, int64_t begin, int64_t end,
+                         float* master, float* m, float* v, const AdamK& h, const float* coef,
+                         int out_mode, void* out_full, const OutPtrs& shards, cudaStream_t st) {
+    auto kern = fused_kernel<NT, GT>;
+    const int64_t vecs = ((end + 7) >> 3) - (begin >> 3);
+    const int64_t grid = grid_for(vecs, kThreads, resident_blocks(kern, kThreads));
+    kern<<<(unsigned)grid, kThreads, 0, st>>>(src, g, begin, end, master, m, v, h, coef,
+                                               out_mode, out_full, shards);
+    return cudaGetLastError();
+  }
+};
+
+}  // namespace
+
+// Partials written by one reduce-scatter call over n elements with N ranks.
+int64_t rs_partials_for(int n, int gdtype, int64_t n_elements) {
+  int64_t out = 0;
+  dispatch<RsGrid>(n, gdtype, n_elements, &out);
+  return out;
+}
+
+cudaError_t launch_reduce_scatter(const RankPtrs& src, int gdtype, const GroupK& g,
+                                  float* reduced, int64_t begin, int64_t end, float scale,
+                                  double* partials, cudaStream_t st) {
+  if (end <= begin) return cudaSuccess;
+  return dispatch<RsLaunch>(g.n, gdtype, src, g, begin, end, reduced, scale, partials, st);
+}
+
+cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64_t begin,
+                         int64_t end, float* master, float* m, float* v, const AdamK& h,
+                         const float* coef, int out_mode, void* out_full,
+                         const OutPtrs& shards, cudaStream_t st) {
+  if (end <= begin) return cudaSuccess;
+  return dispatch<FusedLaunch>(g.n, gdtype, src, g, begin, end, master, m, v, h, coef,
+                               out_mode, out_full, shards, st);
+}
+
+}  // namespace zk
