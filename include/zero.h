@@ -235,6 +235,34 @@ int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const*
  * mod 2^64, over n bf16 bit patterns. */
 int zero_layer_checksum(const void* layer, int64_t n, uint64_t* d_out, zero_stream_t stream);
 
+/* zero_reduce_scatter_norm_static: the pages have no counterpart to this
+ * entry point; it exists for callers that cannot allocate device memory
+ * where they clip (code running under another framework's allocator or
+ * memory budget, where a raw cudaMalloc can fail or fragment the pool, and
+ * loops that must not take the device-wide synchronisation cudaMalloc and
+ * cudaFree can carry).  It computes what zero_reduce_scatter (with
+ * sumsq_partials) followed by zero_grad_norm computes for one window:
+ * reduced[...] over [begin, end), *d_norm and *d_coef; the fp64 partial sums
+ * live in a static array of ZERO_STATIC_PARTIALS (4096, 32 KiB) slots in
+ * this library's device memory, which every GPU that loads the library keeps
+ * until the process exits.  It allocates nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.
+ *   - A window needs zero_rs_partials(plan, gdtype, end-begin) slots; if
+ *     that exceeds ZERO_STATIC_PARTIALS the call returns ZERO_ERANGE and
+ *     launches nothing.  (On a 152-SM GB300 any window needs at most a few
+ *     hundred to 1216 slots.)
+ *   - All calls share the slots; each call writes the slots it reads, so
+ *     nothing needs clearing, but calls that overlap on the GPU race on them.
+ * Errors: as zero_reduce_scatter and zero_grad_norm, plus ERANGE above. */
+#define ZERO_STATIC_PARTIALS 4096
+int zero_reduce_scatter_norm_static(const zero_plan_t* plan, int32_t group,
+                                    const void* const* grads, zero_dtype_t gdtype,
+                                    float* reduced, int64_t begin, int64_t end,
+                                    float grad_scale, float max_norm, float* d_norm,
+                                    float* d_coef, zero_stream_t stream);
+
 /* zero_copy: device-to-device copy of `bytes` (a multiple of 16) with
  * 16-byte loads and stores; measures the achievable HBM copy bandwidth. */
 int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_t stream);

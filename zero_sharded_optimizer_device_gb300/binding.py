@@ -105,6 +105,9 @@ _SIGS = {
     "zero_gather_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
     "zero_layer_checksum": (c_i32, [c_vp, c_i64, c_vp, c_vp]),
     "zero_copy": (c_i32, [c_vp, c_vp, c_i64, c_vp]),
+    "zero_reduce_scatter_norm_static": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_i64, c_i64,
+                                                ctypes.c_float, ctypes.c_float, c_vp, c_vp,
+                                                c_vp]),
 }
 
 _LIB = None
@@ -312,3 +315,13 @@ def zero_layer_checksum(layer, n, d_out, stream=None) -> None:
 
 def zero_copy(dst, src, nbytes, stream=None) -> None:
     _check(_lib().zero_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "zero_copy")
+
+
+def zero_reduce_scatter_norm_static(plan, group, grads, gdtype, reduced, begin, end, grad_scale,
+                                    max_norm, d_norm, d_coef, stream=None) -> None:
+    """zero_reduce_scatter + zero_grad_norm for one window with the fp64
+    partials in the library's static device array: for callers that cannot
+    allocate device memory where they clip (see include/zero.h)."""
+    _check(_lib().zero_reduce_scatter_norm_static(
+        plan, group, _ptr_array(grads), gdtype, _ptr(reduced), begin, end, grad_scale, max_norm,
+        _ptr(d_norm), _ptr(d_coef), _stream(stream)), "zero_reduce_scatter_norm_static")

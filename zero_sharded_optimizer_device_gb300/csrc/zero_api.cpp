@@ -134,6 +134,8 @@ extern "C" const char* zero_strerror(int status) {
 
 extern "C" int zero_last_cuda_error(void) { return g_last_cuda; }
 
+void zk::record_cuda_error(int err) { g_last_cuda = err; }
+
 extern "C" int zero_rs_partials(const zero_plan_t* plan, zero_dtype_t gdtype, int64_t n_elements,
                                 int64_t* n_partials) {
   if (!plan || !n_partials || n_elements < 0) return ZERO_EINVAL;

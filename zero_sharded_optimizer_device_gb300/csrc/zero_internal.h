@@ -80,4 +80,7 @@ cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t 
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Records a CUDA error for zero_last_cuda_error() on this host thread.
+void record_cuda_error(int err);
+
 }  // namespace zk
