@@ -60,7 +60,7 @@ class Case:
     """A workload planned on both sides with its device and host state."""
 
     def __init__(self, numels, n_ranks, align, gdtype, grad_sigma=1e-3, master_sigma=0.02,
-                 seed=1234, heavy_tail=False, groups=None, dev=None, hp=None):
+                 seed=1234, heavy_tail=False, groups=None, dev=None, hp=None, host_state=True):
         import torch
         import zero_sharded_optimizer_device_gb300 as Z
         self.Z = Z
@@ -88,6 +88,8 @@ class Case:
                                   g["flat_off"] + g["psi"])
         self.m = torch.zeros_like(self.master)
         self.v = torch.zeros_like(self.master)
+        if not host_state:          # full-size cases: the oracle works on windows only
+            return
         # host (oracle) state, same generator definition
         self.h_master = np.zeros(P, F32)
         for g in self.groups:
@@ -143,3 +145,47 @@ class Case:
         assert_close_f32(self.master[sl].cpu().numpy(), self.h_master[sl], what + " master", exact)
         assert_close_f32(self.m[sl].cpu().numpy(), self.h_m[sl], what + " m", exact)
         assert_close_f32(self.v[sl].cpu().numpy(), self.h_v[sl], what + " v", exact)
+
+    def oracle_window(self, group: int, window, steps, clip_coefs=None, out_dtype="bf16"):
+        """Run the oracle for `steps` (an iterable of step numbers) on one
+        window of a group, from freshly generated master weights and m = v =
+        0; returns the last step's result dict."""
+        g = self.groups[group]
+        a, b = window
+        f0 = g["flat_off"]
+        master = synth.values(self.seed, synth.MASTER, 0, 0, f0 + a, f0 + b, self.master_sigma,
+                              f0 + g["psi"])
+        m = np.zeros_like(master)
+        v = np.zeros_like(master)
+        r = None
+        for i, s in enumerate(steps):
+            local = self.grads_host(group, s, a, b)
+            coef = None if clip_coefs is None else clip_coefs[i]
+            r = O.zero_step(local, master, m, v, g["shard"], s, self.hp, window=(a, b),
+                            clip_coef=coef, out_dtype=out_dtype)
+            master, m, v = r["master"], r["m"], r["v"]
+        return r
+
+    def check_window(self, group: int, window, r, what: str, exact: bool = True):
+        g = self.groups[group]
+        f0 = g["flat_off"]
+        sl = slice(f0 + window[0], f0 + window[1])
+        assert_close_f32(self.master[sl].cpu().numpy(), r["master"], what + " master", exact)
+        assert_close_f32(self.m[sl].cpu().numpy(), r["m"], what + " m", exact)
+        assert_close_f32(self.v[sl].cpu().numpy(), r["v"], what + " v", exact)
+
+
+def boundary_windows(P: int, cuts, half: int):
+    """Windows of +-half elements around every cut (clipped to [0, P)),
+    merged where they overlap, plus the first and last elements."""
+    ws = [(0, min(P, 2 * half)), (max(0, P - 2 * half), P)]
+    for c in cuts:
+        ws.append((max(0, c - half), min(P, c + half)))
+    ws.sort()
+    out = []
+    for a, b in ws:
+        if out and a <= out[-1][1]:
+            out[-1] = (out[-1][0], max(out[-1][1], b))
+        else:
+            out.append((a, b))
+    return out

@@ -8,7 +8,7 @@ import synth
 from synth import workloads as W
 from oracle import zero_oracle as O
 
-from harness import Case, assert_bf16, assert_close_f32, bits_of
+from harness import Case, assert_bf16, assert_close_f32, bits_of, boundary_windows
 
 pytestmark = pytest.mark.gpu
 
@@ -276,20 +276,15 @@ def test_outputs_stay_inside_their_buffers(cuda):
 
 
 # ------------------------------------------------ full size, sampled windows --
-def _sample_windows(P, S, N, half=4096):
-    ws = [(0, 2 * half), (P - 2 * half, P)]
-    for k in range(1, N):
-        ws.append((k * S - half, k * S + half))
-    return ws
-
-
 def test_gpt2_small_full_size_sampled(cuda):
     """The workload the benchmark times (fused zero_step, N=8, bf16 grads),
-    5 steps at full size; sampled windows across every owner boundary are
-    recomputed by the oracle from generated inputs."""
+    5 steps at full size; sampled windows across every owner boundary and a
+    sample of tensor edges are recomputed by the oracle from generated
+    inputs."""
     import torch
     w = W.GPT2_SMALL
-    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed)
+    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed,
+             host_state=False)
     Z = c.Z
     P, S = c.info["psi_pad"], c.groups[0]["shard"]
     assert P == 124_439_808 and S == 15_554_976
@@ -300,9 +295,8 @@ def test_gpt2_small_full_size_sampled(cuda):
         Z.zero_step(c.plan, 0, grads, Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(s), None, out,
                     Z.ZERO_BF16)
     torch.cuda.synchronize()
-    for a, b in _sample_windows(P, S, w.n_ranks):
-        last = None
-        for s in range(1, w.steps + 1):
-            last = c.oracle_step(0, s, window=(a, b))
-        c.check_state(f"gpt2-small [{a},{b})", sl=slice(a, b))
-        assert_bf16(bits_of(out[a:b]), last["full"], f"gathered [{a},{b})")
+    cuts = [k * S for k in range(1, w.n_ranks)] + np.cumsum(w.numels)[:-1].tolist()[::11]
+    for a, b in boundary_windows(P, cuts, 4096):
+        r = c.oracle_window(0, (a, b), range(1, w.steps + 1))
+        c.check_window(0, (a, b), r, f"gpt2-small [{a},{b})")
+        assert_bf16(bits_of(out[a:b]), r["full"], f"gathered [{a},{b})")
