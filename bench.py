@@ -156,6 +156,21 @@ def profiled_traffic(kernel: str, workload: str):
     return entry.get("bytes_per_launch")
 
 
+def host_mapped(t) -> bool:
+    """True when a pinned host tensor is mapped into the device address space
+    at the same address (so kernels may read and write it directly)."""
+    import ctypes
+    try:
+        rt = ctypes.CDLL("libcudart.so.13")
+    except OSError:
+        return False
+    f = rt.cudaHostGetDevicePointer
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p, ctypes.c_uint]
+    dp = ctypes.c_void_p()
+    return f(ctypes.byref(dp), ctypes.c_void_p(t.data_ptr()), 0) == 0 and dp.value == t.data_ptr()
+
+
 def algorithmic_bytes(n_ranks: int, psi: int, grad_bytes: int) -> int:
     """Bytes one fused step must move: N gradient reads, 12 B of fp32
     master/m/v read and 12 B written, 2 B of bf16 parameters written."""
@@ -242,14 +257,24 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
     launch_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
 
     # end to end through the public API: inputs from pinned host memory,
-    # updated bf16 parameters back to pinned host memory, every step
+    # updated bf16 parameters back to pinned host memory, every step.  When
+    # the pinned buffers are mapped into the device address space (UVA), the
+    # fused kernel reads the gradients and writes the parameters over the
+    # host link itself (zero-copy), which overlaps the transfer with the
+    # step; otherwise explicit copies bracket the step.
     h_grads = [torch.empty(P, dtype=gdt, pin_memory=True) for _ in range(N)]
     for r in range(N):
         h_grads[r].copy_(grads[r])
     h_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
     e2e_steps = max(5, min(50, steps // 20))
+    zero_copy = all(host_mapped(x) for x in h_grads + [h_out])
 
     def e2e_step():
+        if zero_copy:
+            t[0] += 1
+            Z.zero_step(plan, 0, h_grads, zg, master, m, v, Z.adam_hp(t[0], 1.0 / N), None,
+                        h_out, Z.ZERO_BF16, stream)
+            return
         for r in range(N):
             grads[r].copy_(h_grads[r], non_blocking=True)
         step()
@@ -269,7 +294,9 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
 
     return dict(local_ms=local_ms, launch_ms=launch_ms, e2e_ms=e2e_ms, psi=w.psi, psi_pad=P,
                 n_ranks=N, gbytes=gbytes, copy_gbs=copy_gbs, clocks=clocks.summary(),
-                h2d=N * P * gbytes, d2h=P * 2, e2e_steps=e2e_steps)
+                h2d=N * P * gbytes, d2h=P * 2, e2e_steps=e2e_steps,
+                e2e_transfer="zero-copy kernel access to mapped pinned host memory" if zero_copy
+                else "cudaMemcpyAsync from/to pinned host memory")
 
 
 # ----------------------------------------- bucketed pipeline with clipping --
@@ -433,20 +460,36 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist) -> dict:
                  for j, gi in enumerate(order)]
         return sum(_timed_launches(sa, calls))
 
+    def broadcasts_only():
+        """The ZeRO paper's broadcast form of the same gather: each owner in
+        turn sends its shard to every rank -- here one copy launch per owner
+        into the shared layer buffer instead of one all-gather kernel."""
+        calls = []
+        for j, gi in enumerate(order):
+            g = groups[gi]
+            nbytes = g["shard"] * 2
+            for k in range(N):
+                src = shards[k].data_ptr() + g["rank_off"] * 2
+                dst = bufs[j % 2].data_ptr() + k * nbytes
+                calls.append(lambda s=src, d=dst, b=nbytes: Z.zero_copy(d, s, b, sa))
+        return sum(_timed_launches(sa, calls))
+
     for s in range(1, warmup + 1):
         rs_adam_step(s)
         gather_schedule()
-    rs_ms, sched_ms, gonly_ms = [], [], []
+    rs_ms, sched_ms, gonly_ms, bcast_ms = [], [], [], []
     with ClockSampler(dev.index) as clocks:
         dist.barrier()
         for s in range(warmup + 1, warmup + steps + 1):
             rs_ms.append(rs_adam_step(s))
             sched_ms.append(gather_schedule())
             gonly_ms.append(gathers_only())
+            bcast_ms.append(broadcasts_only())
         dist.barrier()
     gather_elems = 2 * sum(g["psi_pad"] for g in groups)
     return dict(rs_ms=statistics.fmean(rs_ms), sched_ms=statistics.fmean(sched_ms),
-                gonly_ms=statistics.fmean(gonly_ms), P=P, N=N, groups=len(groups),
+                gonly_ms=statistics.fmean(gonly_ms), bcast_ms=statistics.fmean(bcast_ms),
+                P=P, N=N, groups=len(groups),
                 gather_elems=gather_elems, clocks=clocks.summary())
 
 
@@ -535,6 +578,8 @@ def secondary_line(w, args, dist) -> dict:
             "rs_adam_gbs": algorithmic_bytes(N, P, 2) / (rs_ms * 1e-3) / 1e9,
             "gather": {"schedule_ms": r["sched_ms"], "gathers_only_ms": r["gonly_ms"],
                        "gather_gbs": 4 * r["gather_elems"] / (r["gonly_ms"] * 1e-3) / 1e9,
+                       "broadcast_ms": r["bcast_ms"],
+                       "broadcast_gbs": 4 * r["gather_elems"] / (r["bcast_ms"] * 1e-3) / 1e9,
                        "schedule_gbs_incl_consumer": 6 * r["gather_elems"] /
                        (r["sched_ms"] * 1e-3) / 1e9},
             "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind},
@@ -630,7 +675,7 @@ def main(argv=None):
         "clocks": res["clocks"],
         "e2e": {"value": e2e_value, "unit": "Gparams/s", "h2d_bytes_per_step": res["h2d"],
                 "d2h_bytes_per_step": res["d2h"], "ms_per_step": e2e_ms,
-                "steps": res["e2e_steps"]},
+                "steps": res["e2e_steps"], "transfer": res.get("e2e_transfer")},
         "gpu_launches": args.steps,
     }
     if args.kernel_only:

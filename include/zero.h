@@ -33,6 +33,11 @@
  *     passed as zero_stream_t; NULL = the legacy default stream).  They
  *     report argument errors and launch errors only; a later
  *     cudaStreamSynchronize reports execution errors.
+ *   - "Device pointer" means any address the GPU can access: device memory,
+ *     or pinned host memory mapped into the device address space (cudaHostAlloc
+ *     on a unified-addressing system).  Given mapped host buffers for grads or
+ *     the gathered output, the kernels read and write them over the host link
+ *     directly, overlapping the transfer with the step.
  *   - Every device pointer must be 16-byte aligned (ZERO_EALIGN otherwise),
  *     except fp64 partial sums (8 bytes) and the checksum word (8 bytes).
  *     Element offsets that break 16-byte vectors (odd windows, align=1
@@ -165,10 +170,27 @@ int zero_plan_volume(const zero_plan_t* plan, int64_t* send_per_rank, int64_t* r
  * ..., k (the owner adds last).  gdtype: ZERO_F32 or ZERO_BF16.
  * If sumsq_partials is not NULL, also writes zero_rs_partials() fp64
  * partial sums of (reduced * grad_scale)^2 over the window, for
- * zero_grad_norm().  Errors: EINVAL, EALIGN, ERANGE, EDTYPE, ECUDA. */
+ * zero_grad_norm().  With reduced == NULL (and sumsq_partials given) only the
+ * partials are produced: the first pass of a fused clip that re-reads the
+ * gradients instead of storing the fp32 reduced gradient (worth it when
+ * N * sizeof(grad) < 8 bytes, i.e. the re-read costs less than the 8-byte
+ * store + load of the reduced value).
+ * Errors: EINVAL (also when both outputs are NULL), EALIGN, ERANGE, EDTYPE,
+ * ECUDA. */
 int zero_reduce_scatter(const zero_plan_t* plan, int32_t group, const void* const* grads,
                         zero_dtype_t gdtype, float* reduced, int64_t begin, int64_t end,
                         float grad_scale, double* sumsq_partials, zero_stream_t stream);
+/* zero_reduce_scatter_acc: gradient accumulation over micro-batches
+ * ["ZeRO Optimizer", "Hybrid Approaches": gradient accumulation with
+ * micro-batching]: reduced[f] = reduced[f] + (ring sum of this micro-batch),
+ * in that order, fp32, for i in [begin, end).  The first micro-batch uses
+ * zero_reduce_scatter; Adam then takes grad_scale = 1/(N * micro_batches).
+ * sumsq_partials (may be NULL) sum (accumulated * grad_scale)^2, so the last
+ * micro-batch's call yields the norm of the accumulated gradient. */
+int zero_reduce_scatter_acc(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                            zero_dtype_t gdtype, float* reduced, int64_t begin, int64_t end,
+                            float grad_scale, double* sumsq_partials, zero_stream_t stream);
+
 /* Number of fp64 partials zero_reduce_scatter writes for a window of
  * n_elements with this plan's N and gdtype on the current device (one per
  * block of its launch; blocks without work write 0). */
@@ -262,6 +284,37 @@ int zero_reduce_scatter_norm_static(const zero_plan_t* plan, int32_t group,
                                     float* reduced, int64_t begin, int64_t end,
                                     float grad_scale, float max_norm, float* d_norm,
                                     float* d_coef, zero_stream_t stream);
+
+/* zero_wait_flag: failure detection without a device fault (no counterpart
+ * on the pages, which have no failure handling).  A one-thread kernel polls
+ * *flag -- device memory, or pinned host memory mapped into the device
+ * address space that the host may write while the kernel runs -- until it
+ * equals `expected` or max_polls polls about 1 us apart have passed, then
+ * writes ZERO_OK or ZERO_ETIMEOUT to *d_status.  The wait always ends, so a
+ * peer that never signals turns into a status the host reads after the
+ * stream synchronizes, and the context stays usable.  0 <= max_polls <=
+ * ZERO_MAX_POLLS (about 10 s).  Never use it to wait for another kernel of
+ * this process: launches are not guaranteed to run concurrently. */
+#define ZERO_MAX_POLLS 10000000
+int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
+                   int32_t* d_status, zero_stream_t stream);
+
+/* zero_set_occupancy: tuning knob (no counterpart on the pages).  Every
+ * streaming kernel runs one wave of 256-thread blocks striding over its
+ * window; this sets how many blocks per SM a kernel family keeps resident
+ * (1..32; 0 restores the library default; the register limit still caps
+ * it).  HBM throughput of these kernels often peaks below full occupancy,
+ * and the best value depends on the kernel and the GPU.  *previous (may be
+ * NULL) receives the value in effect before the call.  Process-wide; set it
+ * between steps, not while a reduce-scatter's partials are still to be
+ * read: zero_rs_partials() follows the setting in effect. */
+#define ZERO_OCC_FUSED 0  /* zero_step, zero_step_group */
+#define ZERO_OCC_RS 1     /* zero_reduce_scatter, zero_reduce_scatter_acc */
+#define ZERO_OCC_ADAM 2   /* zero_adam_shard */
+#define ZERO_OCC_GATHER 3 /* zero_gather_layer, zero_layer_checksum */
+#define ZERO_OCC_STREAM 4 /* zero_all_gather, zero_copy */
+#define ZERO_OCC_KINDS 5
+int zero_set_occupancy(int32_t kind, int32_t blocks_per_sm, int32_t* previous);
 
 /* zero_copy: device-to-device copy of `bytes` (a multiple of 16) with
  * 16-byte loads and stores; measures the achievable HBM copy bandwidth. */

@@ -300,6 +300,14 @@ def ring_all_gather(shards, S: int, window=None):
     return out, sent, recv
 
 
+def accumulate_reduced(prev, reduced):
+    """Gradient accumulation over micro-batches ("ZeRO Optimizer", "Hybrid
+    Approaches": gradient accumulation with micro-batching): each owner keeps
+    the running sum of its reduced chunks, previous micro-batches first,
+    fp32: new = prev + reduced."""
+    return [(p + r).astype(F32) for p, r in zip(prev, reduced)]
+
+
 # ---------------------------------------------------------------------------
 # a3: scale and global-norm clip
 # ---------------------------------------------------------------------------

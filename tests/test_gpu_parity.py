@@ -300,3 +300,32 @@ def test_gpt2_small_full_size_sampled(cuda):
         r = c.oracle_window(0, (a, b), range(1, w.steps + 1))
         c.check_window(0, (a, b), r, f"gpt2-small [{a},{b})")
         assert_bf16(bits_of(out[a:b]), r["full"], f"gathered [{a},{b})")
+
+
+def test_zero_copy_host_buffers_match_device_buffers(cuda):
+    """Pinned host buffers mapped into the device address space may be
+    passed straight to zero_step (the kernel then moves the data over the
+    host link): same results, bit for bit, as device-resident buffers."""
+    import torch
+    import bench
+    w = W.mini(W.GPT2_SMALL, scale=64)
+    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed,
+             host_state=False)
+    Z = c.Z
+    P = c.info["psi_pad"]
+    grads = c.grads_dev(0, 1)
+    h_grads = [torch.empty(P, dtype=torch.bfloat16, pin_memory=True) for _ in range(c.n)]
+    for h, d in zip(h_grads, grads):
+        h.copy_(d)
+    h_out = torch.zeros(P, dtype=torch.bfloat16, pin_memory=True)
+    if not all(bench.host_mapped(x) for x in h_grads + [h_out]):
+        pytest.skip("pinned host memory is not mapped into the device address space")
+    master2, m2, v2 = c.master.clone(), c.m.clone(), c.v.clone()
+    out = torch.zeros(P, dtype=torch.bfloat16, device=cuda)
+    Z.zero_step(c.plan, 0, grads, Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(1), None, out,
+                Z.ZERO_BF16)
+    Z.zero_step(c.plan, 0, h_grads, Z.ZERO_BF16, master2, m2, v2, c.hp_dev(1), None, h_out,
+                Z.ZERO_BF16)
+    torch.cuda.synchronize()
+    assert torch.equal(master2, c.master) and torch.equal(m2, c.m) and torch.equal(v2, c.v)
+    assert torch.equal(h_out, out.cpu())

@@ -408,3 +408,29 @@ def test_planted_mistakes_fail_a_pin(monkeypatch):
     wrong = p0 + 1e-3 * g / (np.abs(g) + F32(1e-8))
     right = p0.astype(np.float64) - 1e-3 * g.astype(np.float64) / (np.abs(g) + 1e-8)
     assert not np.allclose(wrong, right, atol=4e-9)
+
+
+def test_accumulation_over_micro_batches():
+    # exact arithmetic: accumulating M micro-batches' reduce-scatters equals
+    # one reduce-scatter of every rank's summed gradient; with small integer
+    # values every fp32 sum is exact, so the two agree bit for bit
+    rng = np.random.default_rng(10)
+    n, S, M = 4, 6, 3
+    mbs = [[rng.integers(-50, 50, n * S).astype(F32) for _ in range(n)] for _ in range(M)]
+    acc = O.ring_reduce_scatter(mbs[0], S)[0]
+    for mb in mbs[1:]:
+        acc = O.accumulate_reduced(acc, O.ring_reduce_scatter(mb, S)[0])
+    summed = [sum(mb[r] for mb in mbs).astype(F32) for r in range(n)]
+    want = O.ring_reduce_scatter(summed, S)[0]
+    for a, b in zip(acc, want):
+        assert np.array_equal(a, b)
+    # general values: within the recursive-summation bound of the exact sum
+    mbs = [[(rng.standard_normal(n * S) * 1e-3).astype(F32) for _ in range(n)] for _ in range(M)]
+    acc = O.ring_reduce_scatter(mbs[0], S)[0]
+    for mb in mbs[1:]:
+        acc = O.accumulate_reduced(acc, O.ring_reduce_scatter(mb, S)[0])
+    terms = np.stack([x.astype(np.float64) for mb in mbs for x in mb])
+    exact, absum = terms.sum(axis=0), np.abs(terms).sum(axis=0)
+    k = n * M - 1
+    gamma = k * 2.0 ** -24 / (1 - k * 2.0 ** -24)
+    assert np.all(np.abs(np.concatenate(acc).astype(np.float64) - exact) <= gamma * absum)

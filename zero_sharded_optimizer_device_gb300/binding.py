@@ -28,6 +28,8 @@ ZERO_ETIMEOUT = -7
 ZERO_F32 = 0
 ZERO_BF16 = 1
 ZERO_MAX_RANKS = 64
+ZERO_MAX_POLLS = 10_000_000
+ZERO_OCC_FUSED, ZERO_OCC_RS, ZERO_OCC_ADAM, ZERO_OCC_GATHER, ZERO_OCC_STREAM = range(5)
 
 _NAMES = {0: "ZERO_OK", -1: "ZERO_EINVAL", -2: "ZERO_EALIGN", -3: "ZERO_ERANGE",
           -4: "ZERO_EDTYPE", -5: "ZERO_ENOMEM", -6: "ZERO_ECUDA", -7: "ZERO_ETIMEOUT"}
@@ -94,6 +96,8 @@ _SIGS = {
     "zero_rs_partials": (c_i32, [c_vp, c_i32, c_i64, P(c_i64)]),
     "zero_reduce_scatter": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_i64, c_i64,
                                     ctypes.c_float, c_vp, c_vp]),
+    "zero_reduce_scatter_acc": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_i64, c_i64,
+                                        ctypes.c_float, c_vp, c_vp]),
     "zero_grad_norm": (c_i32, [c_vp, c_i64, ctypes.c_float, c_vp, c_vp, c_vp]),
     "zero_adam_shard": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, P(zero_adam_t), c_vp,
                                 c_i64, c_i64, c_vp, c_i32, c_vp]),
@@ -105,6 +109,8 @@ _SIGS = {
     "zero_gather_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
     "zero_layer_checksum": (c_i32, [c_vp, c_i64, c_vp, c_vp]),
     "zero_copy": (c_i32, [c_vp, c_vp, c_i64, c_vp]),
+    "zero_set_occupancy": (c_i32, [c_i32, c_i32, P(c_i32)]),
+    "zero_wait_flag": (c_i32, [c_vp, ctypes.c_uint32, c_i64, c_vp, c_vp]),
     "zero_reduce_scatter_norm_static": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_i64, c_i64,
                                                 ctypes.c_float, ctypes.c_float, c_vp, c_vp,
                                                 c_vp]),
@@ -272,6 +278,13 @@ def zero_reduce_scatter(plan, group, grads, gdtype, reduced, begin, end, grad_sc
                                       _stream(stream)), "zero_reduce_scatter")
 
 
+def zero_reduce_scatter_acc(plan, group, grads, gdtype, reduced, begin, end, grad_scale,
+                            sumsq_partials=None, stream=None) -> None:
+    _check(_lib().zero_reduce_scatter_acc(plan, group, _ptr_array(grads), gdtype, _ptr(reduced),
+                                          begin, end, grad_scale, _ptr(sumsq_partials),
+                                          _stream(stream)), "zero_reduce_scatter_acc")
+
+
 def zero_grad_norm(partials, n, max_norm, d_norm, d_coef, stream=None) -> None:
     _check(_lib().zero_grad_norm(_ptr(partials), n, max_norm, _ptr(d_norm), _ptr(d_coef),
                                  _stream(stream)), "zero_grad_norm")
@@ -311,6 +324,20 @@ def zero_gather_layer(plan, group, shards, dtype, layer_out, stream=None) -> Non
 def zero_layer_checksum(layer, n, d_out, stream=None) -> None:
     _check(_lib().zero_layer_checksum(_ptr(layer), n, _ptr(d_out), _stream(stream)),
            "zero_layer_checksum")
+
+
+def zero_set_occupancy(kind: int, blocks_per_sm: int) -> int:
+    """Set a kernel family's resident blocks per SM (0 = default); returns
+    the previous value."""
+    prev = c_i32()
+    _check(_lib().zero_set_occupancy(kind, blocks_per_sm, ctypes.byref(prev)),
+           "zero_set_occupancy")
+    return prev.value
+
+
+def zero_wait_flag(flag, expected, max_polls, d_status, stream=None) -> None:
+    _check(_lib().zero_wait_flag(_ptr(flag), expected, max_polls, _ptr(d_status),
+                                 _stream(stream)), "zero_wait_flag")
 
 
 def zero_copy(dst, src, nbytes, stream=None) -> None:

@@ -152,12 +152,28 @@ extern "C" int zero_reduce_scatter(const zero_plan_t* plan, int32_t group,
   if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
   ZERO_TRY(check_window(plan, group, begin, end));
   ZERO_TRY(check_rank_ptrs(plan, grads));
+  if (!reduced && !sumsq_partials) return ZERO_EINVAL;  // nothing to produce
+  ZERO_TRY(check_opt_buf(reduced));
+  ZERO_TRY(check_opt_f64(sumsq_partials));
+  return cuda_status(zk::launch_reduce_scatter(
+      rank_ptrs(plan, grads), gdtype, group_k(plan, group), reduced, begin, end, grad_scale,
+      sumsq_partials, reduced ? zk::RS_STORE : zk::RS_NORM_ONLY, (cudaStream_t)stream));
+}
+
+extern "C" int zero_reduce_scatter_acc(const zero_plan_t* plan, int32_t group,
+                                       const void* const* grads, zero_dtype_t gdtype,
+                                       float* reduced, int64_t begin, int64_t end,
+                                       float grad_scale, double* sumsq_partials,
+                                       zero_stream_t stream) {
+  ZERO_TRY(check_group(plan, group));
+  if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_window(plan, group, begin, end));
+  ZERO_TRY(check_rank_ptrs(plan, grads));
   ZERO_TRY(check_buf(reduced));
   ZERO_TRY(check_opt_f64(sumsq_partials));
-  return cuda_status(zk::launch_reduce_scatter(rank_ptrs(plan, grads), gdtype,
-                                               group_k(plan, group), reduced, begin, end,
-                                               grad_scale, sumsq_partials,
-                                               (cudaStream_t)stream));
+  return cuda_status(zk::launch_reduce_scatter(
+      rank_ptrs(plan, grads), gdtype, group_k(plan, group), reduced, begin, end, grad_scale,
+      sumsq_partials, zk::RS_ACCUMULATE, (cudaStream_t)stream));
 }
 
 extern "C" int zero_grad_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
@@ -275,4 +291,12 @@ extern "C" int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_
   ZERO_TRY(check_buf(dst));
   ZERO_TRY(check_buf(src));
   return cuda_status(zk::launch_copy(dst, src, bytes, (cudaStream_t)stream));
+}
+
+extern "C" int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
+                              int32_t* d_status, zero_stream_t stream) {
+  if (!flag || !d_status || max_polls < 0 || max_polls > ZERO_MAX_POLLS) return ZERO_EINVAL;
+  if (((uintptr_t)flag & 3u) != 0 || ((uintptr_t)d_status & 3u) != 0) return ZERO_EALIGN;
+  return cuda_status(zk::launch_wait_flag(flag, expected, max_polls, d_status,
+                                          (cudaStream_t)stream));
 }

@@ -12,6 +12,12 @@ namespace zk {
 
 constexpr int kThreads = 256;
 
+// Resident 256-thread blocks per SM of each kernel family (the grid is one
+// wave: SMs x this cap, or less where the occupancy limit is lower).  The
+// defaults and the measurements behind them are in zero_rs.cu; callers may
+// override them with zero_set_occupancy().
+int occupancy_cap(int kind);
+
 // 16-byte load of data read exactly once (read-only path, no L1 allocation).
 __device__ __forceinline__ uint4 ld_once(const void* p) {
   uint4 r;

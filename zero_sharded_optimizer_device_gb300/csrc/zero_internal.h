@@ -48,10 +48,17 @@ struct AdamK {
 
 enum OutMode : int { OUT_NONE = 0, OUT_FULL_BF16 = 1, OUT_FULL_F32 = 2, OUT_SHARDS_BF16 = 3 };
 
+// What the reduce-scatter does with the ring sum of each element.
+enum RsMode : int {
+  RS_STORE = 0,       // reduced = sum
+  RS_NORM_ONLY = 1,   // only the sum-of-squares partials (reduced untouched)
+  RS_ACCUMULATE = 2,  // reduced = reduced + sum (gradient accumulation)
+};
+
 // Launchers (zero_kernels.cu, zero_rs.cu).  Each returns the launch status.
 cudaError_t launch_reduce_scatter(const RankPtrs& src, int gdtype, const GroupK& g,
                                   float* reduced, int64_t begin, int64_t end, float scale,
-                                  double* partials, cudaStream_t st);
+                                  double* partials, int mode, cudaStream_t st);
 int64_t rs_partials_for(int n, int gdtype, int64_t n_elements);
 
 cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64_t begin,
@@ -76,6 +83,9 @@ cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& 
 cudaError_t launch_checksum(const void* layer, int64_t n, uint64_t* out, cudaStream_t st);
 
 cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t st);
+
+cudaError_t launch_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
+                             int32_t* status, cudaStream_t st);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

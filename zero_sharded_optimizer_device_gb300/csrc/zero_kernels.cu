@@ -15,7 +15,8 @@ namespace zk {
 namespace {
 
 template <typename K>
-int64_t wave_grid(K kernel, int64_t items) {
+int64_t wave_grid(K kernel, int64_t items, int kind) {
+  const int cap = occupancy_cap(kind);
   static std::mutex mu;
   static std::unordered_map<const void*, int> cache[16];
   int dev = 0;
@@ -34,9 +35,10 @@ int64_t wave_grid(K kernel, int64_t items) {
       c[reinterpret_cast<const void*>(kernel)] = nb;
     }
   }
+  if (nb > cap) nb = cap;
   int64_t want = (items + kThreads - 1) / kThreads;
-  const int64_t cap = (int64_t)sm_count() * nb;
-  if (want > cap) want = cap;
+  const int64_t wave = (int64_t)sm_count() * nb;
+  if (want > wave) want = wave;
   return want < 1 ? 1 : want;
 }
 
@@ -105,7 +107,7 @@ cudaError_t launch_adam(const GroupK& g, int64_t begin, int64_t end, float* mast
                         int out_mode, void* out, cudaStream_t st) {
   if (end <= begin) return cudaSuccess;
   const int64_t vecs = ((end + 7) >> 3) - (begin >> 3);
-  adam_kernel<<<(unsigned)wave_grid(adam_kernel, vecs), kThreads, 0, st>>>(
+  adam_kernel<<<(unsigned)wave_grid(adam_kernel, vecs, ZERO_OCC_ADAM), kThreads, 0, st>>>(
       g, begin, end, master, m, v, reduced, h, coef, out_mode, out);
   return cudaGetLastError();
 }
@@ -147,7 +149,7 @@ cudaError_t launch_cast(const float* src, int64_t a, int64_t b, int out_dtype, v
                         cudaStream_t st) {
   if (b <= a) return cudaSuccess;
   const int64_t vecs = ((b + 7) >> 3) - (a >> 3);
-  cast_kernel<<<(unsigned)wave_grid(cast_kernel, vecs), kThreads, 0, st>>>(src, a, b, out_dtype,
+  cast_kernel<<<(unsigned)wave_grid(cast_kernel, vecs, ZERO_OCC_STREAM), kThreads, 0, st>>>(src, a, b, out_dtype,
                                                                            dst);
   return cudaGetLastError();
 }
@@ -220,10 +222,10 @@ cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& 
                           int64_t psi_pad, void* out, cudaStream_t st) {
   if (psi_pad <= 0) return cudaSuccess;
   if (elem_bytes == 2) {
-    gather_kernel<2><<<(unsigned)wave_grid(gather_kernel<2>, psi_pad / 8 + 1), kThreads, 0, st>>>(
+    gather_kernel<2><<<(unsigned)wave_grid(gather_kernel<2>, psi_pad / 8 + 1, ZERO_OCC_GATHER), kThreads, 0, st>>>(
         shards, g, psi_pad, out);
   } else {
-    gather_kernel<4><<<(unsigned)wave_grid(gather_kernel<4>, psi_pad / 4 + 1), kThreads, 0, st>>>(
+    gather_kernel<4><<<(unsigned)wave_grid(gather_kernel<4>, psi_pad / 4 + 1, ZERO_OCC_GATHER), kThreads, 0, st>>>(
         shards, g, psi_pad, out);
   }
   return cudaGetLastError();
@@ -259,7 +261,7 @@ cudaError_t launch_checksum(const void* layer, int64_t n, uint64_t* out, cudaStr
   cudaError_t e = cudaMemsetAsync(out, 0, sizeof(uint64_t), st);
   if (e != cudaSuccess) return e;
   if (n <= 0) return cudaSuccess;
-  checksum_kernel<<<(unsigned)wave_grid(checksum_kernel, n / 8 + 1), kThreads, 0, st>>>(
+  checksum_kernel<<<(unsigned)wave_grid(checksum_kernel, n / 8 + 1, ZERO_OCC_GATHER), kThreads, 0, st>>>(
       static_cast<const uint16_t*>(layer), n, reinterpret_cast<unsigned long long*>(out));
   return cudaGetLastError();
 }
@@ -275,8 +277,35 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t st) {
   const int64_t nv = bytes / 16;
   if (nv <= 0) return cudaSuccess;
-  copy_kernel<<<(unsigned)wave_grid(copy_kernel, nv), kThreads, 0, st>>>(
+  copy_kernel<<<(unsigned)wave_grid(copy_kernel, nv, ZERO_OCC_STREAM), kThreads, 0, st>>>(
       static_cast<uint4*>(dst), static_cast<const uint4*>(src), nv);
+  return cudaGetLastError();
+}
+
+}  // namespace zk
+
+namespace zk {
+
+// ---------------------------------------------------------------------------
+// Bounded wait on a flag (failure detection): poll *flag until it equals
+// `expected` or max_polls polls about 1 us apart have passed; never hangs.
+// ---------------------------------------------------------------------------
+__global__ void wait_flag_kernel(const volatile uint32_t* flag, uint32_t expected,
+                                 int64_t max_polls, int32_t* status) {
+  int32_t st = ZERO_ETIMEOUT;
+  for (int64_t i = 0; i < max_polls; ++i) {
+    if (*flag == expected) {
+      st = ZERO_OK;
+      break;
+    }
+    __nanosleep(1000);
+  }
+  *status = st;
+}
+
+cudaError_t launch_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
+                             int32_t* status, cudaStream_t st) {
+  wait_flag_kernel<<<1, 1, 0, st>>>(flag, expected, max_polls, status);
   return cudaGetLastError();
 }
 

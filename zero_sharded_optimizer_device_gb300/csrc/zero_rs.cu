@@ -12,6 +12,7 @@
 // Both kernels stream: every thread owns 8 consecutive elements per
 // iteration, loads them from the N sources with 16-byte loads, and the grid
 // strides over the window with one resident wave of blocks.
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -50,6 +51,31 @@ int64_t grid_for(int64_t items, int threads, int per_sm) {
 
 }  // namespace
 
+// Occupancy caps (resident 256-thread blocks per SM) of the kernel families.
+// Measured on GB300 with the benchmark's workloads: HBM throughput of these
+// streaming kernels often peaks below full occupancy, because fewer
+// concurrent request streams per SM keep DRAM accesses more local; see the
+// design notes for the sweep.  zero_set_occupancy() overrides them.
+namespace {
+// Best caps of a sweep on GB300 with the workloads' random data (GB/s):
+// fused N=8 step 3 (6699; 6326 at 2, 6097 at 4), fused N=16 3 (7069), Adam
+// 2 (6418; 5775 at 4), reduce-scatter with norm partials 8 (6550-6732;
+// 5780 at 3), stage-3 gather 8 (6522; 4444 at 3), all-gather cast 4 (6494).
+constexpr int kOccDefault[ZERO_OCC_KINDS] = {
+    3,   // ZERO_OCC_FUSED
+    8,   // ZERO_OCC_RS
+    2,   // ZERO_OCC_ADAM
+    8,   // ZERO_OCC_GATHER
+    4,   // ZERO_OCC_STREAM
+};
+std::atomic<int> g_occ[ZERO_OCC_KINDS] = {{0}, {0}, {0}, {0}, {0}};
+}  // namespace
+
+int occupancy_cap(int kind) {
+  const int v = g_occ[kind].load(std::memory_order_relaxed);
+  return v > 0 ? v : kOccDefault[kind];
+}
+
 int sm_count() {
   static int cached[16] = {0};
   int dev = 0;
@@ -70,7 +96,7 @@ int sm_count() {
 template <int NT, typename GT>
 __global__ void __launch_bounds__(kThreads)
     rs_kernel(RankPtrs src, GroupK g, int64_t begin, int64_t end, float* __restrict__ reduced,
-              float scale, double* __restrict__ partials) {
+              float scale, double* __restrict__ partials, int mode) {
   const int n = NT > 0 ? NT : g.n;
   const int64_t q0 = begin >> 3, q1 = (end + 7) >> 3;
   const bool flat_vec_ok = (g.flat_off & 7) == 0;  // 16-byte vectors in flat arrays
@@ -78,12 +104,20 @@ __global__ void __launch_bounds__(kThreads)
   for (int64_t q = q0 + gtid(); q < q1; q += gstride()) {
     const int64_t i = q << 3;
     const int k = owner_of(i, g);
-    float* out = reduced + g.flat_off + i;
+    float* out = reduced + g.flat_off + i;  // not dereferenced in RS_NORM_ONLY
     if (flat_vec_ok && i >= begin && i + 8 <= end && i + 7 < (int64_t)(k + 1) * g.S) {
       float acc[8];
       ring_sum8<NT, GT>(src, n, k, i, acc);
-      st_stream(out, make_float4(acc[0], acc[1], acc[2], acc[3]));
-      st_stream(out + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+      if (mode == RS_ACCUMULATE) {  // previous micro-batches first, then this one
+        const float4 a = ld_state(out), b = ld_state(out + 4);
+        const float prev[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(prev[e], acc[e]);
+      }
+      if (mode != RS_NORM_ONLY) {
+        st_stream(out, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        st_stream(out + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+      }
       if (partials) {
         float s = 0.f;
 #pragma unroll
@@ -98,8 +132,9 @@ __global__ void __launch_bounds__(kThreads)
       for (int e = 0; e < 8; ++e) {
         const int64_t j = i + e;
         if (j < begin || j >= end) continue;
-        const float r = ring_sum1<GT>(src, n, owner_of(j, g), j);
-        out[e] = r;
+        float r = ring_sum1<GT>(src, n, owner_of(j, g), j);
+        if (mode == RS_ACCUMULATE) r = __fadd_rn(out[e], r);
+        if (mode != RS_NORM_ONLY) out[e] = r;
         const float x = __fmul_rn(r, scale);
         s = __fadd_rn(s, __fmul_rn(x, x));
       }
@@ -232,12 +267,15 @@ struct RsLaunch {
   // one resident wave.  The partial count a caller reserves is this grid.
   static int64_t grid(int64_t n_elements) {
     const int64_t vecs = (n_elements + 7) / 8 + 1;
-    return grid_for(vecs, kThreads, resident_blocks(rs_kernel<NT, GT>, kThreads));
+    const int nb = resident_blocks(rs_kernel<NT, GT>, kThreads);
+    const int cap = occupancy_cap(ZERO_OCC_RS);
+    return grid_for(vecs, kThreads, nb < cap ? nb : cap);
   }
   static cudaError_t run(const RankPtrs& src, const GroupK& g, int64_t begin, int64_t end,
-                         float* reduced, float scale, double* partials, cudaStream_t st) {
-    rs_kernel<NT, GT><<<(unsigned)grid(end - begin), kThreads, 0, st>>>(src, g, begin, end,
-                                                                        reduced, scale, partials);
+                         float* reduced, float scale, double* partials, int mode,
+                         cudaStream_t st) {
+    rs_kernel<NT, GT><<<(unsigned)grid(end - begin), kThreads, 0, st>>>(
+        src, g, begin, end, reduced, scale, partials, mode);
     return cudaGetLastError();
   }
 };
@@ -257,7 +295,9 @@ struct FusedLaunch {
                          int out_mode, void* out_full, const OutPtrs& shards, cudaStream_t st) {
     auto kern = fused_kernel<NT, GT>;
     const int64_t vecs = ((end + 7) >> 3) - (begin >> 3);
-    const int64_t grid = grid_for(vecs, kThreads, resident_blocks(kern, kThreads));
+    const int nb = resident_blocks(kern, kThreads);
+    const int cap = occupancy_cap(ZERO_OCC_FUSED);
+    const int64_t grid = grid_for(vecs, kThreads, nb < cap ? nb : cap);
     kern<<<(unsigned)grid, kThreads, 0, st>>>(src, g, begin, end, master, m, v, h, coef,
                                                out_mode, out_full, shards);
     return cudaGetLastError();
@@ -275,9 +315,10 @@ int64_t rs_partials_for(int n, int gdtype, int64_t n_elements) {
 
 cudaError_t launch_reduce_scatter(const RankPtrs& src, int gdtype, const GroupK& g,
                                   float* reduced, int64_t begin, int64_t end, float scale,
-                                  double* partials, cudaStream_t st) {
+                                  double* partials, int mode, cudaStream_t st) {
   if (end <= begin) return cudaSuccess;
-  return dispatch<RsLaunch>(g.n, gdtype, src, g, begin, end, reduced, scale, partials, st);
+  return dispatch<RsLaunch>(g.n, gdtype, src, g, begin, end, reduced, scale, partials, mode,
+                            st);
 }
 
 cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64_t begin,
@@ -290,3 +331,11 @@ cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64
 }
 
 }  // namespace zk
+
+extern "C" int zero_set_occupancy(int32_t kind, int32_t blocks_per_sm, int32_t* previous) {
+  if (kind < 0 || kind >= ZERO_OCC_KINDS || blocks_per_sm < 0 || blocks_per_sm > 32)
+    return ZERO_EINVAL;
+  if (previous) *previous = zk::occupancy_cap(kind);
+  zk::g_occ[kind].store(blocks_per_sm, std::memory_order_relaxed);
+  return ZERO_OK;
+}
