@@ -407,7 +407,7 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist) -> dict:
     shards = [torch.zeros(ST, dtype=torch.bfloat16, device=dev) for _ in range(N)]
     slot = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(N)]
     bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    sums = torch.zeros(2 * len(groups), dtype=torch.int64, device=dev)
+    sums = torch.zeros(2 * len(groups), dtype=torch.int64, device=dev)  # one per gather
     sa = torch.cuda.current_stream(dev)
     sb = torch.cuda.Stream(dev)
 
@@ -429,27 +429,11 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist) -> dict:
     order = list(range(len(groups))) + list(reversed(range(len(groups))))
 
     def gather_schedule():
-        """Prefetch on stream B into the free buffer, consume on stream A."""
-        ready = [torch.cuda.Event() for _ in order]
-        done = [torch.cuda.Event() for _ in order]
+        """Prefetch on stream B into the free buffer, consume on stream A
+        (the library's native two-stream schedule)."""
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(sa)
-        sb.wait_event(e0)
-
-        def issue(j):
-            if j >= 2:
-                sb.wait_event(done[j - 2])
-            gi = order[j]
-            Z.zero_gather_layer(plan, gi, shards, Z.ZERO_BF16, bufs[j % 2], sb)
-            ready[j].record(sb)
-
-        issue(0)
-        for j, gi in enumerate(order):
-            if j + 1 < len(order):
-                issue(j + 1)
-            sa.wait_event(ready[j])
-            Z.zero_layer_checksum(bufs[j % 2], groups[gi]["psi_pad"], sums[j:j + 1], sa)
-            done[j].record(sa)
+        Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, sa, sb)
         e1.record(sa)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
@@ -491,6 +475,59 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist) -> dict:
                 gonly_ms=statistics.fmean(gonly_ms), bcast_ms=statistics.fmean(bcast_ms),
                 P=P, N=N, groups=len(groups),
                 gather_elems=gather_elems, clocks=clocks.summary())
+
+
+# ------------------------------------------- stage-3 gather granularity sweep --
+def regroup(w, per: str):
+    """Layer-group list of the stage-3 workload at another granularity:
+    'tensor' (per-parameter partitioning: every tensor its own group),
+    'layer' (the workload's groups) or 'k-layers' (k consecutive groups)."""
+    if per == "tensor":
+        return list(range(len(w.numels)))
+    if per == "layer":
+        return list(w.groups)
+    k = int(per.split("-")[0])
+    return [g // k for g in w.groups]
+
+
+def bench_gather_sweep(w, steps: int, dist: Dist) -> dict:
+    """Forward + reverse per-group gathers of the stage-3 workload's bf16
+    shards at several partition granularities (the shards are generated
+    directly; no optimizer step is needed to time the gathers)."""
+    import torch
+    import synth
+    import zero_sharded_optimizer_device_gb300 as Z
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    N = w.n_ranks
+    sa = torch.cuda.current_stream(dev)
+    res = {}
+    for per in ("tensor", "layer", "2-layers", "4-layers"):
+        groups_of = regroup(w, per)
+        plan = Z.zero_plan(w.numels, N, w.align, groups_of)
+        info = Z.zero_plan_info(plan)
+        groups = [Z.zero_plan_group(plan, g) for g in range(info["n_groups"])]
+        shards = [torch.empty(info["shard_total"], dtype=torch.bfloat16, device=dev)
+                  for _ in range(N)]
+        for r in range(N):
+            synth.fill_tensor(shards[r], w.seed, synth.MASTER, 0, r, 0, w.master_sigma,
+                              info["shard_total"])
+        gmax = max(g["psi_pad"] for g in groups)
+        bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        order = list(range(len(groups))) + list(reversed(range(len(groups))))
+        calls = [lambda j=j, gi=gi: Z.zero_gather_layer(plan, gi, shards, Z.ZERO_BF16,
+                                                        bufs[j % 2], sa)
+                 for j, gi in enumerate(order)]
+        _timed_launches(sa, calls)                     # warm-up
+        ms = statistics.fmean(sum(_timed_launches(sa, calls)) for _ in range(steps))
+        elems = 2 * sum(g["psi_pad"] for g in groups)
+        res[per] = {"groups": len(groups), "gathers": len(order), "ms": ms,
+                    "gbs": 4 * elems / (ms * 1e-3) / 1e9,
+                    "mean_gather_mb": 2 * elems / len(order) / 1e6}
+        del shards, bufs
+        torch.cuda.empty_cache()
+    return res
 
 
 # ------------------------------------------------- oracle on the host cores --
@@ -599,6 +636,8 @@ def main(argv=None):
                     help="shrink the workload's tensors by this factor (profiling cases)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the step kernel: no copy peak, e2e or CPU baseline")
+    ap.add_argument("--gather-sweep", action="store_true",
+                    help="stage-3 workload: gather bandwidth at several partition granularities")
     args = ap.parse_args(argv)
     from synth import workloads as W
     w = W.ALL[args.workload]
@@ -637,6 +676,13 @@ def main(argv=None):
     assert torch.cuda.is_available(), "bench.py needs a CUDA device"
     import zero_sharded_optimizer_device_gb300  # noqa: F401  (fails loudly when unbuilt)
 
+    if args.gather_sweep:
+        res = bench_gather_sweep(w, max(1, args.steps), dist)
+        if dist.rank == 0:
+            print(json.dumps({"workload": f"{w.name} stage-3 gathers, forward + reverse",
+                              "n_ranks": w.n_ranks, "granularity": res}), flush=True)
+        dist.close()
+        return
     if w.name.startswith("llama-1.4b") or w.name.startswith("llama-7b"):
         line = secondary_line(w, args, dist)
         if dist.rank == 0:

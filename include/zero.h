@@ -252,6 +252,26 @@ int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* g
 int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
                       zero_dtype_t dtype, void* layer_out, zero_stream_t stream);
 
+/* zero_stage3_gather_pass (stage 3) ["ZeRO Optimizer", "Implementation
+ * Strategy": gather a layer's parameters just before use, discard after, in
+ * forward and backward; "Communication Optimization": hide the gathering
+ * behind computation by prefetching the next layer]: for j = 0..n-1, gather
+ * group order[j] (zero_gather_layer) into layer_bufs[j % 2] on stream_b and
+ * consume it on stream_a (zero_layer_checksum into d_sums[j], standing in
+ * for the layer's computation).  The gather of order[j+1] is queued before
+ * the consumer of order[j], so the two overlap; a buffer is refilled only
+ * after the consumer that last read it has finished.  Stream B first waits
+ * for the work already queued on stream A; work queued on stream A after the
+ * call runs after every gather and consumer.  layer_bufs: 2 device buffers
+ * of buf_elems bf16 elements each (>= psi_pad of every group in order);
+ * d_sums: n uint64.  stream_a != stream_b.  Uses four CUDA events created
+ * and released inside the call; allocates no device memory.
+ * Errors: EINVAL, EALIGN, ERANGE (group id or buffer size), ECUDA. */
+int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* order, int32_t n,
+                            const void* const* shards, void* const* layer_bufs,
+                            int64_t buf_elems, uint64_t* d_sums, zero_stream_t stream_a,
+                            zero_stream_t stream_b);
+
 /* zero_layer_checksum: stands in for the layer computation that consumes a
  * gathered buffer: *d_out = sum over j < n of bits[j] * (1 + j mod 65536)
  * mod 2^64, over n bf16 bit patterns. */

@@ -147,31 +147,13 @@ def test_llama_7b_stage3_full_size(cuda):
                 e = min(win[1], j + 64, (k + 1) * S)
                 got = bits_of(shards[k][ro + j - k * S:ro + e - k * S])
                 assert_bf16(got, full[j - win[0]:e - win[0]], f"shard {k} group {gi}")
-    # gathers: the same two-stream schedule as the benchmark
-    sa = torch.cuda.current_stream()
+    # gathers: the native two-stream schedule the benchmark times
     sb = torch.cuda.Stream()
     bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=cuda) for _ in range(2)]
     order = list(range(G)) + list(reversed(range(G)))
     sums = torch.zeros(len(order), dtype=torch.int64, device=cuda)
-    ready = [torch.cuda.Event() for _ in order]
-    done = [torch.cuda.Event() for _ in order]
-    start = torch.cuda.Event()
-    start.record(sa)
-    sb.wait_event(start)
-
-    def issue(j):
-        if j >= 2:
-            sb.wait_event(done[j - 2])
-        Z.zero_gather_layer(c.plan, order[j], shards, Z.ZERO_BF16, bufs[j % 2], sb)
-        ready[j].record(sb)
-
-    issue(0)
-    for j, gi in enumerate(order):
-        if j + 1 < len(order):
-            issue(j + 1)
-        sa.wait_event(ready[j])
-        Z.zero_layer_checksum(bufs[j % 2], c.groups[gi]["psi_pad"], sums[j:j + 1], sa)
-        done[j].record(sa)
+    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums,
+                              torch.cuda.current_stream(), sb)
     torch.cuda.synchronize()
     # property at any size: each gathered layer is the concatenation of the
     # owners' shards, checksummed by plain PyTorch integer arithmetic

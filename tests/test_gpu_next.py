@@ -150,3 +150,74 @@ def test_occupancy_setting_does_not_change_results(cuda):
         for a, b in zip(r[:5], base[:5]):
             assert torch.equal(a, b)
         assert abs(r[5] - base[5]) <= 1e-6 * base[5]
+
+
+def test_stage3_per_parameter_partitioning(cuda):
+    """Per-parameter partitioning (each tensor its own group, sharded over
+    the N ranks and padded on its own): step and gather of every tensor
+    match the oracle."""
+    import torch
+    d, ffn, vocab = 48, 130, 301
+    numels = [vocab * d] + [d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] + [d, vocab * d]
+    groups = list(range(len(numels)))
+    c = Case(numels, 16, 8, "bf16", seed=91, groups=groups)
+    Z = c.Z
+    N = 16
+    assert c.info["n_groups"] == len(numels)
+    shards = [torch.zeros(c.info["shard_total"], dtype=torch.bfloat16, device=cuda)
+              for _ in range(N)]
+    for gi in reversed(range(len(c.groups))):
+        Z.zero_step_group(c.plan, gi, c.grads_dev(gi, 1), Z.ZERO_BF16, c.master, c.m, c.v,
+                          c.hp_dev(1), None, shards)
+        c.oracle_step(gi, 1)
+    torch.cuda.synchronize()
+    c.check_state("per-parameter stage 3")
+    for gi, g in enumerate(c.groups):
+        layer = torch.empty(g["psi_pad"], dtype=torch.bfloat16, device=cuda)
+        Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, layer)
+        torch.cuda.synchronize()
+        f0 = g["flat_off"]
+        assert_bf16(bits_of(layer), O.f32_to_bf16(c.h_master[f0:f0 + g["psi_pad"]]),
+                    f"tensor {gi}")
+
+
+def test_native_gather_schedule_matches_direct_gathers(cuda):
+    """zero_stage3_gather_pass (gathers on stream B, consumer on stream A,
+    double-buffered) yields, for every gather of a forward + reverse pass,
+    the checksum of the directly gathered layer; and rejects bad input."""
+    import torch
+    d, ffn, vocab = 64, 172, 500
+    blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(3)]
+    numels = [vocab * d] + [n for b in blocks for n in b] + [d, vocab * d]
+    groups = [0] + [1 + i // 9 for i in range(27)] + [4, 4]
+    c = Case(numels, 16, 16, "bf16", seed=5, groups=groups, host_state=False)
+    Z = c.Z
+    N, G = 16, len(c.groups)
+    shards = [torch.empty(c.info["shard_total"], dtype=torch.bfloat16, device=cuda)
+              for _ in range(N)]
+    for r in range(N):
+        shards[r].copy_(torch.randn(c.info["shard_total"], device=cuda).to(torch.bfloat16))
+    gmax = max(g["psi_pad"] for g in c.groups)
+    bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=cuda) for _ in range(2)]
+    order = list(range(G)) + list(reversed(range(G)))
+    sums = torch.zeros(len(order), dtype=torch.int64, device=cuda)
+    sb = torch.cuda.Stream()
+    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums,
+                              torch.cuda.current_stream(), sb)
+    torch.cuda.synchronize()
+    for j, gi in enumerate(order):
+        g = c.groups[gi]
+        layer = torch.empty(g["psi_pad"], dtype=torch.bfloat16, device=cuda)
+        Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, layer)
+        torch.cuda.synchronize()
+        bits = layer.cpu().view(torch.int16).numpy().view(np.uint16)
+        assert int(sums[j].item()) % (1 << 64) == O.layer_checksum(bits), (j, gi)
+    E = Z.ZeroError
+    for bad, status in [(dict(order=[G]), Z.ZERO_ERANGE), (dict(buf_elems=10), Z.ZERO_ERANGE),
+                        (dict(stream_b=torch.cuda.current_stream()), Z.ZERO_EINVAL)]:
+        kw = dict(order=order, buf_elems=gmax, stream_b=sb)
+        kw.update(bad)
+        with pytest.raises(E) as e:
+            Z.zero_stage3_gather_pass(c.plan, kw["order"], shards, bufs, kw["buf_elems"], sums,
+                                      torch.cuda.current_stream(), kw["stream_b"])
+        assert e.value.status == status

@@ -108,6 +108,8 @@ _SIGS = {
                                 P(zero_adam_t), c_vp, P(c_vp), c_vp]),
     "zero_gather_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
     "zero_layer_checksum": (c_i32, [c_vp, c_i64, c_vp, c_vp]),
+    "zero_stage3_gather_pass": (c_i32, [c_vp, P(c_i32), c_i32, P(c_vp), P(c_vp), c_i64, c_vp,
+                                        c_vp, c_vp]),
     "zero_copy": (c_i32, [c_vp, c_vp, c_i64, c_vp]),
     "zero_set_occupancy": (c_i32, [c_i32, c_i32, P(c_i32)]),
     "zero_wait_flag": (c_i32, [c_vp, ctypes.c_uint32, c_i64, c_vp, c_vp]),
@@ -319,6 +321,15 @@ def zero_step_group(plan, group, grads, gdtype, master, m, v, hp, d_coef, shards
 def zero_gather_layer(plan, group, shards, dtype, layer_out, stream=None) -> None:
     _check(_lib().zero_gather_layer(plan, group, _ptr_array(shards), dtype, _ptr(layer_out),
                                     _stream(stream)), "zero_gather_layer")
+
+
+def zero_stage3_gather_pass(plan, order, shards, layer_bufs, buf_elems, d_sums, stream_a,
+                            stream_b) -> None:
+    arr = (c_i32 * max(1, len(order)))(*[int(g) for g in order])
+    _check(_lib().zero_stage3_gather_pass(plan, arr, len(order), _ptr_array(shards),
+                                          _ptr_array(layer_bufs), buf_elems, _ptr(d_sums),
+                                          _stream(stream_a), _stream(stream_b)),
+           "zero_stage3_gather_pass")
 
 
 def zero_layer_checksum(layer, n, d_out, stream=None) -> None:

@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libzero.so")
 
-SOURCES = ["zero_plan.cpp", "zero_api.cpp", "zero_rs.cu", "zero_kernels.cu", "zero_noalloc.cu"]
+SOURCES = ["zero_plan.cpp", "zero_api.cpp", "zero_sched.cpp", "zero_rs.cu", "zero_kernels.cu",
+           "zero_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-I", INCLUDE, "-I", CSRC,
           "-Xcompiler", "-fPIC,-ffp-contract=off,-O2"]

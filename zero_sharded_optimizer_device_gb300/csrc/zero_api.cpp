@@ -4,9 +4,18 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "zero_internal.h"
 
 namespace {
+
+// An NVTX range around each device entry point, so that timeline profilers
+// show which C-ABI call launched which kernel (a no-op without a tool).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 thread_local int g_last_cuda = 0;
 
@@ -148,6 +157,7 @@ extern "C" int zero_reduce_scatter(const zero_plan_t* plan, int32_t group,
                                    const void* const* grads, zero_dtype_t gdtype, float* reduced,
                                    int64_t begin, int64_t end, float grad_scale,
                                    double* sumsq_partials, zero_stream_t stream) {
+  NvtxRange nvtx("zero_reduce_scatter");
   ZERO_TRY(check_group(plan, group));
   if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
   ZERO_TRY(check_window(plan, group, begin, end));
@@ -165,6 +175,7 @@ extern "C" int zero_reduce_scatter_acc(const zero_plan_t* plan, int32_t group,
                                        float* reduced, int64_t begin, int64_t end,
                                        float grad_scale, double* sumsq_partials,
                                        zero_stream_t stream) {
+  NvtxRange nvtx("zero_reduce_scatter_acc");
   ZERO_TRY(check_group(plan, group));
   if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
   ZERO_TRY(check_window(plan, group, begin, end));
@@ -178,6 +189,7 @@ extern "C" int zero_reduce_scatter_acc(const zero_plan_t* plan, int32_t group,
 
 extern "C" int zero_grad_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
                               float* d_coef, zero_stream_t stream) {
+  NvtxRange nvtx("zero_grad_norm");
   if (n < 0 || (n > 0 && !partials) || !isfinite(max_norm) || max_norm <= 0.0f)
     return ZERO_EINVAL;
   ZERO_TRY(check_opt_f64(partials));
@@ -190,6 +202,7 @@ extern "C" int zero_adam_shard(const zero_plan_t* plan, int32_t group, float* ma
                                float* v, const float* reduced, const zero_adam_t* hp,
                                const float* d_coef, int64_t begin, int64_t end, void* out,
                                zero_dtype_t out_dtype, zero_stream_t stream) {
+  NvtxRange nvtx("zero_adam_shard");
   ZERO_TRY(check_group(plan, group));
   ZERO_TRY(check_window(plan, group, begin, end));
   ZERO_TRY(check_buf(master));
@@ -209,6 +222,7 @@ extern "C" int zero_adam_shard(const zero_plan_t* plan, int32_t group, float* ma
 
 extern "C" int zero_all_gather(const zero_plan_t* plan, int32_t group, const float* master,
                                void* full_out, zero_dtype_t out_dtype, zero_stream_t stream) {
+  NvtxRange nvtx("zero_all_gather");
   if (!plan) return ZERO_EINVAL;
   if (group != -1) ZERO_TRY(check_group(plan, group));
   if (!dtype_ok(out_dtype)) return ZERO_EDTYPE;
@@ -226,6 +240,7 @@ extern "C" int zero_step(const zero_plan_t* plan, int32_t group, const void* con
                          zero_dtype_t gdtype, float* master, float* m, float* v,
                          const zero_adam_t* hp, const float* d_coef, void* full_out,
                          zero_dtype_t out_dtype, zero_stream_t stream) {
+  NvtxRange nvtx("zero_step");
   ZERO_TRY(check_group(plan, group));
   if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
   ZERO_TRY(check_rank_ptrs(plan, grads));
@@ -249,6 +264,7 @@ extern "C" int zero_step_group(const zero_plan_t* plan, int32_t group, const voi
                                zero_dtype_t gdtype, float* master, float* m, float* v,
                                const zero_adam_t* hp, const float* d_coef, void* const* shards,
                                zero_stream_t stream) {
+  NvtxRange nvtx("zero_step_group");
   ZERO_TRY(check_group(plan, group));
   if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
   ZERO_TRY(check_rank_ptrs(plan, grads));
@@ -268,6 +284,7 @@ extern "C" int zero_step_group(const zero_plan_t* plan, int32_t group, const voi
 
 extern "C" int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
                                  zero_dtype_t dtype, void* layer_out, zero_stream_t stream) {
+  NvtxRange nvtx("zero_gather_layer");
   ZERO_TRY(check_group(plan, group));
   if (!dtype_ok(dtype)) return ZERO_EDTYPE;
   ZERO_TRY(check_rank_ptrs(plan, shards));
@@ -279,6 +296,7 @@ extern "C" int zero_gather_layer(const zero_plan_t* plan, int32_t group, const v
 
 extern "C" int zero_layer_checksum(const void* layer, int64_t n, uint64_t* d_out,
                                    zero_stream_t stream) {
+  NvtxRange nvtx("zero_layer_checksum");
   if (n < 0 || !d_out || (n > 0 && !layer)) return ZERO_EINVAL;
   ZERO_TRY(check_opt_buf(layer));
   if (((uintptr_t)d_out & 7u) != 0) return ZERO_EALIGN;
@@ -286,6 +304,7 @@ extern "C" int zero_layer_checksum(const void* layer, int64_t n, uint64_t* d_out
 }
 
 extern "C" int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_t stream) {
+  NvtxRange nvtx("zero_copy");
   if (bytes < 0 || (bytes % 16) != 0) return ZERO_EINVAL;
   if (bytes == 0) return ZERO_OK;
   ZERO_TRY(check_buf(dst));
@@ -295,6 +314,7 @@ extern "C" int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_
 
 extern "C" int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
                               int32_t* d_status, zero_stream_t stream) {
+  NvtxRange nvtx("zero_wait_flag");
   if (!flag || !d_status || max_polls < 0 || max_polls > ZERO_MAX_POLLS) return ZERO_EINVAL;
   if (((uintptr_t)flag & 3u) != 0 || ((uintptr_t)d_status & 3u) != 0) return ZERO_EALIGN;
   return cuda_status(zk::launch_wait_flag(flag, expected, max_polls, d_status,

@@ -1,0 +1,100 @@
+// Stage-3 gather schedule on two streams.
+//
+// ["ZeRO Optimizer", "Implementation Strategy"]: stage 3 gathers a layer's
+// parameters just before they are used and discards them afterwards, in the
+// forward and again in the backward pass; "Communication Optimization":
+// parameter gathering is hidden behind computation by prefetching the next
+// layer.  Here the gather of the next group runs on stream B into the free
+// one of two layer buffers while stream A consumes the current one.
+#include <nvtx3/nvToolsExt.h>
+#include <stdint.h>
+
+#include "zero_internal.h"
+
+namespace {
+
+struct Events {
+  cudaEvent_t e[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  cudaError_t create() {
+    for (auto& x : e) {
+      cudaError_t r = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+  }
+  ~Events() {
+    // destroying an event that is still pending is allowed: its resources
+    // are released once it completes
+    for (auto& x : e)
+      if (x) cudaEventDestroy(x);
+  }
+};
+
+}  // namespace
+
+extern "C" int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* order, int32_t n,
+                                       const void* const* shards, void* const* layer_bufs,
+                                       int64_t buf_elems, uint64_t* d_sums,
+                                       zero_stream_t stream_a, zero_stream_t stream_b) {
+  if (!plan || n < 0 || (n > 0 && (!order || !layer_bufs || !d_sums)) || !shards)
+    return ZERO_EINVAL;
+  if (n == 0) return ZERO_OK;
+  if (stream_a == stream_b) return ZERO_EINVAL;
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    if (!shards[r]) return ZERO_EINVAL;
+    if ((uintptr_t)shards[r] & 15u) return ZERO_EALIGN;
+  }
+  for (int b = 0; b < 2; ++b) {
+    if (!layer_bufs[b]) return ZERO_EINVAL;
+    if ((uintptr_t)layer_bufs[b] & 15u) return ZERO_EALIGN;
+  }
+  if ((uintptr_t)d_sums & 7u) return ZERO_EALIGN;
+  for (int32_t j = 0; j < n; ++j) {
+    if (order[j] < 0 || order[j] >= (int32_t)plan->groups.size()) return ZERO_ERANGE;
+    if (plan->groups[order[j]].psi_pad > buf_elems) return ZERO_ERANGE;
+  }
+  nvtxRangePushA("zero_stage3_gather_pass");
+  cudaStream_t sa = (cudaStream_t)stream_a, sb = (cudaStream_t)stream_b;
+  zk::RankPtrs src{};
+  for (int r = 0; r < plan->n_ranks; ++r) src.p[r] = shards[r];
+  Events ev;  // 0: start; 1, 2: gather j ready (slot j%2); 3, 4: consumer j done
+  cudaError_t e = ev.create();
+  auto gk = [&](int32_t g) {
+    const zero_group_info_t& gi = plan->groups[g];
+    zk::GroupK k;
+    k.S = gi.shard;
+    k.flat_off = gi.flat_off;
+    k.rank_off = gi.rank_off;
+    k.invS = gi.shard > 0 ? 1.0f / (float)gi.shard : 0.0f;
+    k.n = plan->n_ranks;
+    return k;
+  };
+  // gather j into buffer j%2 on stream B, once the consumer of j-2 is done
+  auto issue = [&](int32_t j) -> cudaError_t {
+    cudaError_t r = cudaSuccess;
+    if (j >= 2) r = cudaStreamWaitEvent(sb, ev.e[3 + (j & 1)], 0);
+    if (r == cudaSuccess)
+      r = zk::launch_gather(src, 2, gk(order[j]), plan->groups[order[j]].psi_pad,
+                            layer_bufs[j & 1], sb);
+    if (r == cudaSuccess) r = cudaEventRecord(ev.e[1 + (j & 1)], sb);
+    return r;
+  };
+  // stream B starts after everything already queued on stream A (the step
+  // that wrote the shards)
+  if (e == cudaSuccess) e = cudaEventRecord(ev.e[0], sa);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(sb, ev.e[0], 0);
+  if (e == cudaSuccess) e = issue(0);
+  for (int32_t j = 0; j < n && e == cudaSuccess; ++j) {
+    if (j + 1 < n) e = issue(j + 1);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(sa, ev.e[1 + (j & 1)], 0);
+    if (e == cudaSuccess)
+      e = zk::launch_checksum(layer_bufs[j & 1], plan->groups[order[j]].psi_pad, d_sums + j, sa);
+    if (e == cudaSuccess) e = cudaEventRecord(ev.e[3 + (j & 1)], sa);
+  }
+  nvtxRangePop();
+  if (e != cudaSuccess) {
+    zk::record_cuda_error((int)e);
+    return ZERO_ECUDA;
+  }
+  return ZERO_OK;
+}
