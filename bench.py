@@ -133,11 +133,22 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str = "fused_kernel") -> str:
+    """Hash of what decides a kernel's DRAM traffic: the device helpers, the
+    kernel's own source text and the occupancy defaults (host code around it
+    does not count)."""
+    csrc = os.path.join(ROOT, "zero_sharded_optimizer_device_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("zero_rs.cu", "zero_device.cuh", "zero_kernels.cu"):
-        with open(os.path.join(ROOT, "zero_sharded_optimizer_device_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    with open(os.path.join(csrc, "zero_device.cuh"), "rb") as f:
+        h.update(f.read())
+    with open(os.path.join(csrc, "zero_rs.cu")) as f:
+        text = f.read()
+    start = text.index(f"    {kernel}(")
+    start = text.rindex("template", 0, start)
+    end = text.index("// ------", start)
+    h.update(text[start:end].encode())
+    occ = text.index("constexpr int kOccDefault")
+    h.update(text[occ:text.index("};", occ)].encode())
     return h.hexdigest()[:16]
 
 
@@ -151,7 +162,7 @@ def profiled_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     entry = rec.get(workload, {}).get(kernel)
-    if not entry or entry.get("source_hash") != kernel_source_hash():
+    if not entry or entry.get("source_hash") != kernel_source_hash(kernel):
         return None
     return entry.get("bytes_per_launch")
 
@@ -539,6 +550,7 @@ def oracle_sample(w, target_s: float, max_steps: int | None = None, window: int 
     import synth
     from oracle import zero_oracle as O
 
+    pin_to_one_core()
     p = O.plan(w.numels, w.n_ranks, w.align)
     S = p.groups[0].shard
     win = window or min(p.psi_pad, 1 << 20)
@@ -565,6 +577,15 @@ def oracle_sample(w, target_s: float, max_steps: int | None = None, window: int 
     desc = (f"oracle fused step on elements [{a},{b}) of {w.name} (N={w.n_ranks}, owner 0/1 "
             f"boundary), {steps} steps, single-threaded numpy")
     return win * steps / el, desc, steps, el
+
+
+def pin_to_one_core() -> None:
+    """Run the oracle on one host core (the baseline is single-threaded)."""
+    try:
+        cores = sorted(os.sched_getaffinity(0))
+        os.sched_setaffinity(0, {cores[-1]})
+    except (AttributeError, OSError):
+        pass
 
 
 def cpu_model() -> str:

@@ -90,6 +90,10 @@ cudaError_t launch_wait_flag(const uint32_t* flag, uint32_t expected, int64_t ma
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Resident blocks per SM of `kernel` at `threads` per block on the current
+// device (the occupancy limit; cached per device and kernel).
+int occupancy_of(const void* kernel, int threads);
+
 // Records a CUDA error for zero_last_cuda_error() on this host thread.
 void record_cuda_error(int err);
 

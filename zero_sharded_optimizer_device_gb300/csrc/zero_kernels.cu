@@ -5,9 +5,6 @@
 //   gather_kernel   stage-3 per-layer gather of N rank shards
 //   checksum_kernel consumer of a gathered layer
 //   copy_kernel     16-byte device copy (achievable HBM bandwidth)
-#include <mutex>
-#include <unordered_map>
-
 #include "zero_device.cuh"
 
 namespace zk {
@@ -17,24 +14,7 @@ namespace {
 template <typename K>
 int64_t wave_grid(K kernel, int64_t items, int kind) {
   const int cap = occupancy_cap(kind);
-  static std::mutex mu;
-  static std::unordered_map<const void*, int> cache[16];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int nb = 0;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto& c = cache[dev & 15];
-    auto it = c.find(reinterpret_cast<const void*>(kernel));
-    if (it != c.end()) {
-      nb = it->second;
-    } else {
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess ||
-          nb < 1)
-        nb = 1;
-      c[reinterpret_cast<const void*>(kernel)] = nb;
-    }
-  }
+  int nb = occupancy_of(reinterpret_cast<const void*>(kernel), kThreads);
   if (nb > cap) nb = cap;
   int64_t want = (items + kThreads - 1) / kThreads;
   const int64_t wave = (int64_t)sm_count() * nb;

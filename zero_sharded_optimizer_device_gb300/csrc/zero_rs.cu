@@ -13,8 +13,9 @@
 // iteration, loads them from the N sources with 16-byte loads, and the grid
 // strides over the window with one resident wave of blocks.
 #include <atomic>
+#include <map>
 #include <mutex>
-#include <unordered_map>
+#include <utility>
 
 #include "zero_device.cuh"
 
@@ -22,24 +23,9 @@ namespace zk {
 
 namespace {
 
-// Resident blocks per SM for a kernel (cached per kernel and device).
 template <typename K>
 int resident_blocks(K kernel, int threads) {
-  static std::mutex mu;
-  static std::unordered_map<const void*, int> cache[16];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const void* key = reinterpret_cast<const void*>(kernel);
-  std::lock_guard<std::mutex> lock(mu);
-  auto& c = cache[dev & 15];
-  auto it = c.find(key);
-  if (it != c.end()) return it->second;
-  int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess ||
-      nb < 1)
-    nb = 1;
-  c[key] = nb;
-  return nb;
+  return occupancy_of(reinterpret_cast<const void*>(kernel), threads);
 }
 
 int64_t grid_for(int64_t items, int threads, int per_sm) {
@@ -76,17 +62,38 @@ int occupancy_cap(int kind) {
   return v > 0 ? v : kOccDefault[kind];
 }
 
+namespace {
+std::mutex g_dev_mu;
+std::map<int, int> g_sms;                                // device -> SM count
+std::map<std::pair<int, const void*>, int> g_resident;   // (device, kernel) -> blocks/SM
+}  // namespace
+
 int sm_count() {
-  static int cached[16] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  int& c = cached[dev & 15];
-  if (c == 0) {
-    int s = 0;
-    cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev);
-    c = s > 0 ? s : 1;
-  }
-  return c;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  auto it = g_sms.find(dev);
+  if (it != g_sms.end()) return it->second;
+  int s = 0;
+  if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || s < 1)
+    s = 1;
+  g_sms[dev] = s;
+  return s;
+}
+
+int occupancy_of(const void* kernel, int threads) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  auto key = std::make_pair(dev, kernel);
+  auto it = g_resident.find(key);
+  if (it != g_resident.end()) return it->second;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess ||
+      nb < 1)
+    nb = 1;
+  g_resident[key] = nb;
+  return nb;
 }
 
 // ---------------------------------------------------------------------------
