@@ -167,6 +167,20 @@ def profiled_traffic(kernel: str, workload: str):
     return entry.get("bytes_per_launch")
 
 
+def pinned_host_buffer(nbytes: int):
+    """One page-locked host byte buffer of exactly nbytes (torch's pinned
+    allocator would round each tensor up to a power of two)."""
+    import numpy as np
+    import torch
+    arr = np.empty(nbytes, dtype=np.uint8)
+    rc = torch.cuda.cudart().cudaHostRegister(arr.ctypes.data, nbytes, 0)
+    if int(rc) != 0:
+        raise RuntimeError(f"cudaHostRegister failed ({rc})")
+    t = torch.from_numpy(arr)
+    t._pinned_owner = arr          # keep the numpy buffer alive with the tensor
+    return t
+
+
 def host_mapped(t) -> bool:
     """True when a pinned host tensor is mapped into the device address space
     at the same address (so kernels may read and write it directly)."""
@@ -268,19 +282,29 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
     launch_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
 
     # end to end through the public API: inputs from pinned host memory,
-    # updated bf16 parameters back to pinned host memory, every step.  When
-    # the pinned buffers are mapped into the device address space (UVA), the
-    # fused kernel reads the gradients and writes the parameters over the
-    # host link itself (zero-copy), which overlaps the transfer with the
-    # step; otherwise explicit copies bracket the step.
-    h_grads = [torch.empty(P, dtype=gdt, pin_memory=True) for _ in range(N)]
+    # updated bf16 parameters back to pinned host memory, every step.  Two
+    # ways: explicit copies around the step, or -- when the pinned buffers
+    # are mapped into the device address space -- zero_step on the host
+    # buffers themselves, so the kernel moves the data over the host link
+    # while it streams the state (zero-copy).  Both are timed; the faster is
+    # reported with its mode.
+    host_bytes = N * P * gbytes + P * 2
+    ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    if host_bytes > 0.4 * ram:      # too large to pin on this host: no end-to-end leg
+        return dict(local_ms=local_ms, launch_ms=launch_ms, e2e_ms=None, psi=w.psi, psi_pad=P,
+                    n_ranks=N, gbytes=gbytes, copy_gbs=copy_gbs, clocks=clocks.summary(),
+                    h2d=N * P * gbytes, d2h=P * 2, e2e_steps=0,
+                    e2e_transfer=f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
+                                 f"exceeds 40% of the host's {ram / 1e9:.0f} GB")
+    pinned = pinned_host_buffer(host_bytes)
+    h_grads = [pinned[r * P * gbytes:(r + 1) * P * gbytes].view(gdt) for r in range(N)]
     for r in range(N):
         h_grads[r].copy_(grads[r])
-    h_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
+    h_out = pinned[N * P * gbytes:].view(torch.bfloat16)
     e2e_steps = max(5, min(50, steps // 20))
-    zero_copy = all(host_mapped(x) for x in h_grads + [h_out])
+    mapped = all(host_mapped(x) for x in h_grads + [h_out])
 
-    def e2e_step():
+    def e2e_step(zero_copy):
         if zero_copy:
             t[0] += 1
             Z.zero_step(plan, 0, h_grads, zg, master, m, v, Z.adam_hp(t[0], 1.0 / N), None,
@@ -291,17 +315,27 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
         step()
         h_out.copy_(out, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    dist.barrier()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    s1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    def e2e_time(zero_copy):
+        for _ in range(2):
+            e2e_step(zero_copy)
+        torch.cuda.synchronize()
+        dist.barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step(zero_copy)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        return s0.elapsed_time(s1) / e2e_steps
+
+    # both ways a user can hand host buffers to the library; report the faster
+    modes = {False: e2e_time(False)}
+    if mapped:
+        modes[True] = e2e_time(True)
+    zero_copy = min(modes, key=modes.get)
+    e2e_ms = modes[zero_copy]
+    del h_grads, h_out
+    torch.cuda.cudart().cudaHostUnregister(pinned.data_ptr())
 
     return dict(local_ms=local_ms, launch_ms=launch_ms, e2e_ms=e2e_ms, psi=w.psi, psi_pad=P,
                 n_ranks=N, gbytes=gbytes, copy_gbs=copy_gbs, clocks=clocks.summary(),
@@ -339,7 +373,9 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist) -> dict:
     plan = Z.zero_plan(w.numels, w.n_ranks, w.align)
     P, N = Z.zero_plan_info(plan)["psi_pad"], w.n_ranks
     bucket, chunk = w.extra["bucket"], w.extra["chunk"]
-    grads = [torch.empty(P, dtype=torch.bfloat16, device=dev) for _ in range(N)]
+    gdt = torch.bfloat16 if w.grad_dtype == "bf16" else torch.float32
+    zg = Z.ZERO_BF16 if w.grad_dtype == "bf16" else Z.ZERO_F32
+    grads = [torch.empty(P, dtype=gdt, device=dev) for _ in range(N)]
     for r in range(N):
         synth.fill_tensor(grads[r], w.seed, synth.GRAD, 1, r, 0, w.grad_sigma, w.psi, w.heavy_tail)
     master = torch.empty(P, dtype=torch.float32, device=dev)
@@ -349,7 +385,7 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist) -> dict:
     out = torch.empty(P, dtype=torch.bfloat16, device=dev)
     windows = [(a, min(P, a + bucket)) for a in range(0, P, bucket)]
     chunks = [(a, min(P, a + chunk)) for a in range(0, P, chunk)]
-    npart = [Z.zero_rs_partials(plan, Z.ZERO_BF16, b - a) for a, b in windows]
+    npart = [Z.zero_rs_partials(plan, zg, b - a) for a, b in windows]
     offs = [sum(npart[:i]) for i in range(len(npart))]
     partials = torch.zeros(sum(npart), dtype=torch.float64, device=dev)
     norm = torch.zeros(1, dtype=torch.float32, device=dev)
@@ -363,7 +399,7 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist) -> dict:
         cs = []
         for (a, b), o, k in zip(windows, offs, npart):
             cs.append(lambda a=a, b=b, o=o, k=k: Z.zero_reduce_scatter(
-                plan, 0, grads, Z.ZERO_BF16, reduced, a, b, 1.0 / N, partials[o:o + k], stream))
+                plan, 0, grads, zg, reduced, a, b, 1.0 / N, partials[o:o + k], stream))
         cs.append(lambda: Z.zero_grad_norm(partials, partials.numel(), w.extra["max_norm"], norm,
                                            coef, stream))
         for a, b in chunks:
@@ -607,8 +643,9 @@ def secondary_line(w, args, dist) -> dict:
         r = bench_bucketed(w, args.steps, args.warmup, dist)
         ms = dist.max(r["local_ms"])
         P, N = r["P"], r["N"]
-        formula = algorithmic_bytes(N, P, 2)              # 2N + 26 B/param
-        path = P * ((2 * N + 4) + (4 + 24 + 2))           # RS 2N+4, Adam 30
+        gb = 2 if w.grad_dtype == "bf16" else 4
+        formula = algorithmic_bytes(N, P, gb)             # N*gb + 26 B/param
+        path = P * ((gb * N + 4) + (4 + 24 + 2))          # RS N*gb+4, Adam 30
         return {"metric": METRIC, "value": n_gpus * w.psi / (ms * 1e-3) / 1e9,
                 "unit": "Gparams/s", "n_gpus": n_gpus, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -618,7 +655,7 @@ def secondary_line(w, args, dist) -> dict:
                 "hbm_gbs_formula": formula / (ms * 1e-3) / 1e9,
                 "hbm_gbs_path": path / (ms * 1e-3) / 1e9,
                 "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind,
-                             "rs_gbs": P * (2 * N + 4) / (r["rs_ms"] * 1e-3) / 1e9,
+                             "rs_gbs": P * (gb * N + 4) / (r["rs_ms"] * 1e-3) / 1e9,
                              "adam_gbs": P * 30 / (r["adam_ms"] * 1e-3) / 1e9,
                              "rs_ms": r["rs_ms"], "adam_ms": r["adam_ms"], "norm_ms": r["norm_ms"]},
                 "norm": r["norm"], "clip_coef": r["coef"], "clocks": r["clocks"],
@@ -657,6 +694,8 @@ def main(argv=None):
                     help="shrink the workload's tensors by this factor (profiling cases)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the step kernel: no copy peak, e2e or CPU baseline")
+    ap.add_argument("--grad-dtype", choices=["bf16", "f32"], default=None,
+                    help="override the workload's gradient dtype (fp32 doubles the source bytes)")
     ap.add_argument("--gather-sweep", action="store_true",
                     help="stage-3 workload: gather bandwidth at several partition granularities")
     args = ap.parse_args(argv)
@@ -664,6 +703,10 @@ def main(argv=None):
     w = W.ALL[args.workload]
     if args.scale > 1:
         w = W.mini(w, scale=args.scale)
+    if args.grad_dtype and args.grad_dtype != w.grad_dtype:
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}-{args.grad_dtype}-grads",
+                                grad_dtype=args.grad_dtype)
     dist = Dist()
 
     if args.impl == "reference":
@@ -713,10 +756,10 @@ def main(argv=None):
 
     res = bench_fused(w, args.steps, args.warmup, dist, args.kernel_only)
     ms = dist.max(res["local_ms"])
-    e2e_ms = dist.max(res["e2e_ms"])
+    e2e_ms = dist.max(res["e2e_ms"]) if res["e2e_ms"] is not None else None
     n_gpus = dist.world
     value = n_gpus * w.psi / (ms * 1e-3) / 1e9
-    e2e_value = n_gpus * w.psi / (e2e_ms * 1e-3) / 1e9
+    e2e_value = n_gpus * w.psi / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None
     abytes = algorithmic_bytes(res["n_ranks"], res["psi_pad"], res["gbytes"])
     peak, peak_kind = measured_hbm_peak()
     achieved = abytes / (res["launch_ms"] * 1e-3) / 1e9
@@ -735,7 +778,7 @@ def main(argv=None):
         "hbm_gbs": step_gbs, "hbm_pct_of_peak": 100.0 * step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "fused_kernel<8,bf16>",
+                     "kernel": f"fused_kernel<{res['n_ranks']},{w.grad_dtype}>",
                      "algorithmic_bytes_per_launch": abytes,
                      "traffic": profiled_traffic("fused_kernel", w.name)},
         "copy_peak_gbs": res["copy_gbs"],

@@ -173,3 +173,26 @@ def test_llama_7b_stage3_full_size(cuda):
     g = c.groups[last]
     cat = torch.cat([shards[k][g["rank_off"]:g["rank_off"] + g["shard"]] for k in range(N)])
     assert torch.equal(bufs[0][:g["psi_pad"]], cat)
+
+
+def test_one_group_beyond_2_31_elements(cuda):
+    """Maximum-size edge: one group of 2^31 + 12,345 parameters (N = 2, so
+    the owner boundary also lies above 2^30 and the flat indices pass 2^31);
+    fused step, windows around 2^31, the owner boundary and the ragged end."""
+    import torch
+    psi = (1 << 31) + 12_345
+    c = Case([psi - 1000, 1000], 2, 16, "bf16", seed=2024, host_state=False)
+    Z = c.Z
+    P, S = c.info["psi_pad"], c.groups[0]["shard"]
+    assert P > (1 << 31) and P == 2 * S
+    out = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    grads = c.grads_dev(0, 1)
+    Z.zero_step(c.plan, 0, grads, Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(1), None, out,
+                Z.ZERO_BF16)
+    torch.cuda.synchronize()
+    for a, b in [(0, 64), (S - 40, S + 40), ((1 << 31) - 37, (1 << 31) + 51),
+                 (psi - 1003, psi + 5), (P - 64, P)]:
+        r = c.oracle_window(0, (a, b), (1,))
+        c.check_window(0, (a, b), r, f"2^31 group [{a},{b})")
+        assert_bf16(bits_of(out[a:b]), r["full"], f"gathered [{a},{b})")
+    del grads
