@@ -168,17 +168,22 @@ def profiled_traffic(kernel: str, workload: str):
 
 
 def pinned_host_buffer(nbytes: int):
-    """One page-locked host byte buffer of exactly nbytes (torch's pinned
-    allocator would round each tensor up to a power of two)."""
-    import numpy as np
+    """One page-locked host byte buffer of exactly nbytes from cudaHostAlloc
+    (torch's pinned allocator would round each tensor up to a power of two).
+    Returns (uint8 tensor over it, function that frees it)."""
+    import ctypes
     import torch
-    arr = np.empty(nbytes, dtype=np.uint8)
-    rc = torch.cuda.cudart().cudaHostRegister(arr.ctypes.data, nbytes, 0)
-    if int(rc) != 0:
-        raise RuntimeError(f"cudaHostRegister failed ({rc})")
-    t = torch.from_numpy(arr)
-    t._pinned_owner = arr          # keep the numpy buffer alive with the tensor
-    return t
+    rt = ctypes.CDLL("libcudart.so.13")
+    rt.cudaHostAlloc.restype = ctypes.c_int
+    rt.cudaHostAlloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, ctypes.c_uint]
+    rt.cudaFreeHost.restype = ctypes.c_int
+    rt.cudaFreeHost.argtypes = [ctypes.c_void_p]
+    ptr = ctypes.c_void_p()
+    rc = rt.cudaHostAlloc(ctypes.byref(ptr), nbytes, 0)
+    if rc != 0:
+        raise RuntimeError(f"cudaHostAlloc of {nbytes} bytes failed ({rc})")
+    t = torch.frombuffer((ctypes.c_uint8 * nbytes).from_address(ptr.value), dtype=torch.uint8)
+    return t, (lambda: rt.cudaFreeHost(ptr))
 
 
 def host_mapped(t) -> bool:
@@ -296,7 +301,7 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
                     h2d=N * P * gbytes, d2h=P * 2, e2e_steps=0,
                     e2e_transfer=f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
                                  f"exceeds 40% of the host's {ram / 1e9:.0f} GB")
-    pinned = pinned_host_buffer(host_bytes)
+    pinned, free_pinned = pinned_host_buffer(host_bytes)
     h_grads = [pinned[r * P * gbytes:(r + 1) * P * gbytes].view(gdt) for r in range(N)]
     for r in range(N):
         h_grads[r].copy_(grads[r])
@@ -334,8 +339,8 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
         modes[True] = e2e_time(True)
     zero_copy = min(modes, key=modes.get)
     e2e_ms = modes[zero_copy]
-    del h_grads, h_out
-    torch.cuda.cudart().cudaHostUnregister(pinned.data_ptr())
+    del h_grads, h_out, pinned
+    free_pinned()
 
     return dict(local_ms=local_ms, launch_ms=launch_ms, e2e_ms=e2e_ms, psi=w.psi, psi_pad=P,
                 n_ranks=N, gbytes=gbytes, copy_gbs=copy_gbs, clocks=clocks.summary(),

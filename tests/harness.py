@@ -27,7 +27,9 @@ def assert_close_f32(got: np.ndarray, want: np.ndarray, what: str, exact: bool =
     got = np.asarray(got, dtype=np.float32)
     want = np.asarray(want, dtype=np.float32)
     assert got.shape == want.shape, (what, got.shape, want.shape)
-    bad = ~(np.abs(got.astype(np.float64) - want) <= 1e-7 + 1e-5 * np.abs(want.astype(np.float64)))
+    with np.errstate(invalid="ignore"):
+        bad = ~(np.abs(got.astype(np.float64) - want) <= 1e-7 + 1e-5 * np.abs(want.astype(np.float64)))
+    bad &= ~(got == want)                          # equal infinities
     bad &= ~(np.isnan(got) & np.isnan(want))
     if bad.any():
         i = int(np.flatnonzero(bad)[0])

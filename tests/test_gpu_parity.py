@@ -329,3 +329,91 @@ def test_zero_copy_host_buffers_match_device_buffers(cuda):
     torch.cuda.synchronize()
     assert torch.equal(master2, c.master) and torch.equal(m2, c.m) and torch.equal(v2, c.v)
     assert torch.equal(h_out, out.cpu())
+
+
+def test_large_step_numbers(cuda):
+    """Step numbers where 1 - beta^t has reached 1 in fp32 (and beta1^t has
+    underflowed): the bias corrections agree with the oracle's."""
+    import torch
+    c = Case([5_000, 333], 4, 16, "f32", grad_sigma=1e-2, seed=8)
+    Z = c.Z
+    out = torch.empty(c.info["psi_pad"], dtype=torch.bfloat16, device=cuda)
+    for t in (10_000, 100_000, 1_000_001):
+        Z.zero_step(c.plan, 0, c.grads_dev(0, t), Z.ZERO_F32, c.master, c.m, c.v, c.hp_dev(t),
+                    None, out, Z.ZERO_BF16)
+        r = c.oracle_step(0, t)
+    torch.cuda.synchronize()
+    c.check_state("large t")
+    assert_bf16(bits_of(out), r["full"], "large t gathered")
+
+
+def test_stage3_unaligned_shards(cuda):
+    """align = 1 with N = 3: shard sizes and rank offsets are not multiples
+    of 8, so the step writes owner shards element by element and the gather
+    copies element by element."""
+    import torch
+    numels = [101, 57, 33, 1000, 7]
+    groups = [0, 0, 1, 1, 2]
+    c = Case(numels, 3, 1, "bf16", seed=13, groups=groups)
+    Z = c.Z
+    assert any(g["shard"] % 8 or g["rank_off"] % 8 for g in c.groups)
+    shards = [torch.zeros(c.info["shard_total"], dtype=torch.bfloat16, device=cuda)
+              for _ in range(3)]
+    for gi in range(len(c.groups)):
+        Z.zero_step_group(c.plan, gi, c.grads_dev(gi, 1), Z.ZERO_BF16, c.master, c.m, c.v,
+                          c.hp_dev(1), None, shards)
+        c.oracle_step(gi, 1)
+    torch.cuda.synchronize()
+    c.check_state("stage3 align 1")
+    for gi, g in enumerate(c.groups):
+        layer = torch.empty(g["psi_pad"], dtype=torch.bfloat16, device=cuda)
+        Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, layer)
+        torch.cuda.synchronize()
+        f0 = g["flat_off"]
+        assert_bf16(bits_of(layer), O.f32_to_bf16(c.h_master[f0:f0 + g["psi_pad"]]),
+                    f"group {gi}")
+
+
+def test_non_finite_gradients_propagate_like_the_oracle(cuda):
+    """A NaN or an infinity in one rank's gradient poisons exactly the
+    elements it touches, on both sides; every other element stays
+    bit-identical to the oracle."""
+    import torch
+    c = Case([4096], 4, 16, "f32", grad_sigma=1e-2, seed=17)
+    Z = c.Z
+    grads = c.grads_dev(0, 1)
+    bad = {10: float("nan"), 777: float("inf"), 2048: float("-inf")}
+    for i, x in bad.items():
+        grads[i % 4][i] = x
+    out = torch.empty(c.info["psi_pad"], dtype=torch.bfloat16, device=cuda)
+    Z.zero_step(c.plan, 0, grads, Z.ZERO_F32, c.master, c.m, c.v, c.hp_dev(1), None, out,
+                Z.ZERO_BF16)
+    local = c.grads_host(0, 1)
+    for i, x in bad.items():
+        local[i % 4][i] = np.float32(x)
+    with np.errstate(invalid="ignore"):          # inf/inf on the poisoned elements
+        r = O.zero_step(local, c.h_master, c.h_m, c.h_v, c.groups[0]["shard"], 1, c.hp)
+    torch.cuda.synchronize()
+    got = c.master.cpu().numpy()
+    nan_g, nan_w = np.isnan(got), np.isnan(r["master"])
+    assert np.array_equal(nan_g, nan_w) and nan_w[list(bad)].all()
+    ok = ~nan_w
+    assert_close_f32(got[ok], r["master"][ok], "finite master")
+    assert_close_f32(c.m.cpu().numpy()[ok], r["m"][ok], "finite m")
+    ob = bits_of(out)
+    assert_bf16(ob[ok], r["full"][ok], "finite gathered")
+    assert np.isnan(O.bf16_to_f32(ob[nan_w])).all()
+
+
+def test_zero_gradients_leave_parameters_unchanged(cuda):
+    import torch
+    c = Case([3000, 17], 8, 16, "bf16", seed=19, host_state=False)
+    Z = c.Z
+    grads = [torch.zeros(c.info["psi_pad"], dtype=torch.bfloat16, device=cuda) for _ in range(8)]
+    before = c.master.clone()
+    out = torch.empty(c.info["psi_pad"], dtype=torch.bfloat16, device=cuda)
+    Z.zero_step(c.plan, 0, grads, Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(1), None, out,
+                Z.ZERO_BF16)
+    torch.cuda.synchronize()
+    assert torch.equal(before, c.master) and not c.m.any() and not c.v.any()
+    assert torch.equal(out, before.to(torch.bfloat16))
