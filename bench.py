@@ -208,7 +208,8 @@ def algorithmic_bytes(n_ranks: int, psi: int, grad_bytes: int) -> int:
 
 
 # --------------------------------------------------------- our GPU arm ----
-def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = False) -> dict:
+def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = False,
+                graph: bool = False) -> dict:
     import torch
     import synth
     import zero_sharded_optimizer_device_gb300 as Z
@@ -241,6 +242,37 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
+
+    if graph:
+        # one step captured once -- advance the device-resident Adam step
+        # state, then the fused kernel -- and replayed every step
+        state = torch.zeros(4, dtype=torch.float64, device=dev)
+        hp = Z.adam_hp(t[0] + 1, 1.0 / N, d_state=state)
+        Z.zero_adam_state_init(hp, state, stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side), torch.cuda.graph(g, stream=side):
+            Z.zero_adam_state_advance(hp, state, side)
+            Z.zero_step(plan, 0, grads, zg, master, m, v, hp, None, out, Z.ZERO_BF16, side)
+        stream.wait_stream(side)
+        for _ in range(3):
+            g.replay()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(dev.index) as clocks:
+            dist.barrier()
+            torch.cuda.synchronize()
+            t0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            dist.barrier()
+        ms = t0.elapsed_time(t1) / steps
+        return dict(local_ms=ms, launch_ms=ms, e2e_ms=None, psi=w.psi, psi_pad=P, n_ranks=N,
+                    gbytes=gbytes, copy_gbs=None, clocks=clocks.summary(), h2d=0, d2h=0,
+                    e2e_steps=0, e2e_transfer="not measured with --graph", graph=True)
 
     if kernel_only:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -699,6 +731,8 @@ def main(argv=None):
                     help="shrink the workload's tensors by this factor (profiling cases)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the step kernel: no copy peak, e2e or CPU baseline")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay one CUDA-graph-captured step (device-resident Adam step state)")
     ap.add_argument("--grad-dtype", choices=["bf16", "f32"], default=None,
                     help="override the workload's gradient dtype (fp32 doubles the source bytes)")
     ap.add_argument("--gather-sweep", action="store_true",
@@ -759,7 +793,7 @@ def main(argv=None):
         dist.close()
         return
 
-    res = bench_fused(w, args.steps, args.warmup, dist, args.kernel_only)
+    res = bench_fused(w, args.steps, args.warmup, dist, args.kernel_only, args.graph)
     ms = dist.max(res["local_ms"])
     e2e_ms = dist.max(res["e2e_ms"]) if res["e2e_ms"] is not None else None
     n_gpus = dist.world
@@ -791,8 +825,10 @@ def main(argv=None):
         "e2e": {"value": e2e_value, "unit": "Gparams/s", "h2d_bytes_per_step": res["h2d"],
                 "d2h_bytes_per_step": res["d2h"], "ms_per_step": e2e_ms,
                 "steps": res["e2e_steps"], "transfer": res.get("e2e_transfer")},
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps if res.get("graph") else args.steps,
     }
+    if res.get("graph"):
+        line["config"]["launch"] = "one CUDA graph per step: Adam state advance + fused kernel"
     if args.kernel_only:
         line = {"kernel_only": True, "workload": w.name, "psi": w.psi, "ms_per_step": ms,
                 "value": value, "unit": "Gparams/s", "roofline": line["roofline"]}

@@ -114,8 +114,15 @@ typedef struct {
 typedef struct {
   float lr, beta1, beta2, eps, weight_decay;
   float grad_scale; /* multiplies the reduced sum; 1/N averages */
-  int64_t step;     /* t >= 1: this update's step number */
+  int64_t step;     /* t >= 1: this update's step number (ignored with d_state) */
+  /* NULL, or a ZERO_ADAM_STATE_BYTES device buffer set up by
+   * zero_adam_state_init: the kernels then take the bias corrections from it
+   * instead of from `step`, so one captured CUDA graph of a step stays valid
+   * for every later step (advance it with zero_adam_state_advance). */
+  void* d_state;
 } zero_adam_t;
+
+#define ZERO_ADAM_STATE_BYTES 32
 
 /* ------------------------------------------------------------- library -- */
 int zero_version(void);
@@ -204,6 +211,19 @@ int zero_rs_partials(const zero_plan_t* plan, zero_dtype_t gdtype, int64_t n_ele
  * clip_grad_norm_ applies. */
 int zero_grad_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
                    float* d_coef, zero_stream_t stream);
+
+/* zero_adam_state_init / zero_adam_state_advance: Adam's step-dependent
+ * constants kept in device memory (no counterpart on the pages; it lets a
+ * whole step be captured once in a CUDA graph and replayed).  d_state is a
+ * caller-owned, 8-byte aligned device buffer of ZERO_ADAM_STATE_BYTES.
+ * init sets it to "before step hp->step"; each advance (a one-thread
+ * kernel on `stream`, enqueue it before the step's kernels) moves to the next
+ * step: beta^t is multiplied once more by each fp32 beta in fp64 (stopping
+ * once below 2^-60, exactly as the host computation of zero_adam_t.step
+ * does) and bc = 1 - beta^t is rounded to fp32, so results are bit-identical
+ * to passing the step number.  Errors: EINVAL, EALIGN, ECUDA. */
+int zero_adam_state_init(const zero_adam_t* hp, void* d_state, zero_stream_t stream);
+int zero_adam_state_advance(const zero_adam_t* hp, void* d_state, zero_stream_t stream);
 
 /* zero_adam_shard [P1 "Problem"; P4 "Memory Components"; KB]: for i in
  * [begin, end) of group g (flat index f = flat_off(g) + i):

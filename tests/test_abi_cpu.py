@@ -126,6 +126,12 @@ def test_device_call_argument_errors_return_before_any_launch():
     assert status(Z.zero_wait_flag, A, 1, Z.ZERO_MAX_POLLS + 1, A) == Z.ZERO_EINVAL
     assert status(Z.zero_wait_flag, A + 2, 1, 10, A) == Z.ZERO_EALIGN
     assert status(Z.zero_wait_flag, 0, 1, 10, A) == Z.ZERO_EINVAL
+    assert status(Z.zero_adam_state_init, hp, A + 4) == Z.ZERO_EALIGN
+    assert status(Z.zero_adam_state_init, hp, 0) == Z.ZERO_EINVAL
+    assert status(Z.zero_adam_state_init, Z.adam_hp(0, 0.25), A) == Z.ZERO_EINVAL
+    assert status(Z.zero_adam_state_advance, Z.adam_hp(1, 0.25, beta2=1.5), A) == Z.ZERO_EINVAL
+    assert status(Z.zero_step, p, 0, good, Z.ZERO_BF16, A, A, A,
+                  Z.adam_hp(1, 0.25, d_state=A + 2), None, A) == Z.ZERO_EALIGN
 
 
 def test_rs_partials_requires_known_dtype():

@@ -221,3 +221,124 @@ def test_native_gather_schedule_matches_direct_gathers(cuda):
             Z.zero_stage3_gather_pass(c.plan, kw["order"], shards, bufs, kw["buf_elems"], sums,
                                       torch.cuda.current_stream(), kw["stream_b"])
         assert e.value.status == status
+
+
+def _eager_and_state_cases(w, seed):
+    a = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, seed,
+             host_state=False)
+    b = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, seed,
+             host_state=False)
+    return a, b
+
+
+def test_device_adam_state_matches_step_numbers(cuda):
+    import torch
+    w = W.mini(W.GPT2_SMALL, scale=256)
+    a, b = _eager_and_state_cases(w, 41)
+    Z = a.Z
+    P = a.info["psi_pad"]
+    out_a = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    out_b = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    state = torch.zeros(Z.ZERO_ADAM_STATE_BYTES // 8, dtype=torch.float64, device=cuda)
+    hp_dev = Z.adam_hp(step=5000, grad_scale=1.0 / a.n, d_state=state)
+    Z.zero_adam_state_init(hp_dev, state)            # "before step 5000"
+    for t in range(5000, 5003):
+        g = a.grads_dev(0, t)
+        Z.zero_step(a.plan, 0, g, Z.ZERO_BF16, a.master, a.m, a.v, a.hp_dev(t), None, out_a)
+        Z.zero_adam_state_advance(hp_dev, state)
+        Z.zero_step(b.plan, 0, g, Z.ZERO_BF16, b.master, b.m, b.v, hp_dev, None, out_b)
+    torch.cuda.synchronize()
+    assert torch.equal(a.master, b.master) and torch.equal(a.m, b.m) and torch.equal(a.v, b.v)
+    assert torch.equal(out_a, out_b)
+
+
+def test_cuda_graph_of_a_fused_step_replays_exactly(cuda):
+    """One step (advance the device Adam state, fused zero_step) captured in a
+    CUDA graph and replayed three times equals three eager steps."""
+    import torch
+    w = W.mini(W.GPT2_SMALL, scale=256)
+    a, b = _eager_and_state_cases(w, 43)
+    Z = a.Z
+    P = a.info["psi_pad"]
+    grads = a.grads_dev(0, 1)
+    out_a = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    out_b = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    for t in range(1, 4):
+        Z.zero_step(a.plan, 0, grads, Z.ZERO_BF16, a.master, a.m, a.v, a.hp_dev(t), None, out_a)
+    state = torch.zeros(4, dtype=torch.float64, device=cuda)
+    hp = Z.adam_hp(step=1, grad_scale=1.0 / b.n, d_state=state)
+    # warm-up on scratch copies so that every launch parameter is cached
+    sm, smm, sv = b.master.clone(), b.m.clone(), b.v.clone()
+    Z.zero_adam_state_init(hp, state)
+    Z.zero_adam_state_advance(hp, state)
+    Z.zero_step(b.plan, 0, grads, Z.ZERO_BF16, sm, smm, sv, hp, None, out_b)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            Z.zero_adam_state_advance(hp, state)
+            Z.zero_step(b.plan, 0, grads, Z.ZERO_BF16, b.master, b.m, b.v, hp, None, out_b)
+    torch.cuda.current_stream().wait_stream(s)
+    Z.zero_adam_state_init(hp, state)                  # back to "before step 1"
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(a.master, b.master) and torch.equal(a.m, b.m) and torch.equal(a.v, b.v)
+    assert torch.equal(out_a, out_b)
+
+
+def test_cuda_graph_of_the_bucketed_clip_pipeline(cuda):
+    """Reduce-scatter buckets with norm partials, device norm and clip,
+    chunked Adam and the state advance captured once; two replays equal two
+    eager steps bit for bit."""
+    import torch
+    w = W.mini(W.LLAMA_1_4B, scale=1024)
+    a, b = (Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma,
+                 w.seed, heavy_tail=True, host_state=False) for _ in range(2))
+    Z = a.Z
+    P = a.info["psi_pad"]
+    grads = a.grads_dev(0, 1)
+    bucket, chunk = 100_003, 400_001
+    windows = [(x, min(P, x + bucket)) for x in range(0, P, bucket)]
+    chunks = [(x, min(P, x + chunk)) for x in range(0, P, chunk)]
+    npart = [Z.zero_rs_partials(a.plan, Z.ZERO_BF16, hi - lo) for lo, hi in windows]
+
+    def buffers():
+        return (torch.empty(P, dtype=torch.float32, device=cuda),
+                torch.zeros(sum(npart), dtype=torch.float64, device=cuda),
+                torch.zeros(1, dtype=torch.float32, device=cuda),
+                torch.empty(P, dtype=torch.bfloat16, device=cuda))
+
+    def step(c, red, part, coef, out, hp):
+        off = 0
+        for (lo, hi), k in zip(windows, npart):
+            Z.zero_reduce_scatter(c.plan, 0, grads, Z.ZERO_BF16, red, lo, hi, 1.0 / c.n,
+                                  part[off:off + k])
+            off += k
+        Z.zero_grad_norm(part, off, 1.0, None, coef)
+        for lo, hi in chunks:
+            Z.zero_adam_shard(c.plan, 0, c.master, c.m, c.v, red, hp, coef, lo, hi, out)
+
+    ba = buffers()
+    for t in (1, 2):
+        step(a, *ba, a.hp_dev(t))
+    bb = buffers()
+    state = torch.zeros(4, dtype=torch.float64, device=cuda)
+    hp = Z.adam_hp(step=1, grad_scale=1.0 / b.n, d_state=state)
+    Z.zero_adam_state_init(hp, state)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            Z.zero_adam_state_advance(hp, state)
+            step(b, *bb, hp)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(a.master, b.master) and torch.equal(a.m, b.m) and torch.equal(a.v, b.v)
+    assert torch.equal(ba[3], bb[3]) and torch.equal(ba[2], bb[2])

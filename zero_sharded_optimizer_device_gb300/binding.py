@@ -72,12 +72,16 @@ class zero_mem_t(ctypes.Structure):
 class zero_adam_t(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
-                ("grad_scale", ctypes.c_float), ("step", c_i64)]
+                ("grad_scale", ctypes.c_float), ("step", c_i64), ("d_state", c_vp)]
+
+
+ZERO_ADAM_STATE_BYTES = 32
 
 
 def adam_hp(step: int, grad_scale: float, lr: float = 1e-3, beta1: float = 0.9,
-            beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0) -> zero_adam_t:
-    return zero_adam_t(lr, beta1, beta2, eps, weight_decay, grad_scale, step)
+            beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
+            d_state=None) -> zero_adam_t:
+    return zero_adam_t(lr, beta1, beta2, eps, weight_decay, grad_scale, step, _ptr(d_state))
 
 
 _SIGS = {
@@ -111,6 +115,8 @@ _SIGS = {
     "zero_stage3_gather_pass": (c_i32, [c_vp, P(c_i32), c_i32, P(c_vp), P(c_vp), c_i64, c_vp,
                                         c_vp, c_vp]),
     "zero_copy": (c_i32, [c_vp, c_vp, c_i64, c_vp]),
+    "zero_adam_state_init": (c_i32, [P(zero_adam_t), c_vp, c_vp]),
+    "zero_adam_state_advance": (c_i32, [P(zero_adam_t), c_vp, c_vp]),
     "zero_set_occupancy": (c_i32, [c_i32, c_i32, P(c_i32)]),
     "zero_wait_flag": (c_i32, [c_vp, ctypes.c_uint32, c_i64, c_vp, c_vp]),
     "zero_reduce_scatter_norm_static": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_i64, c_i64,
@@ -335,6 +341,16 @@ def zero_stage3_gather_pass(plan, order, shards, layer_bufs, buf_elems, d_sums, 
 def zero_layer_checksum(layer, n, d_out, stream=None) -> None:
     _check(_lib().zero_layer_checksum(_ptr(layer), n, _ptr(d_out), _stream(stream)),
            "zero_layer_checksum")
+
+
+def zero_adam_state_init(hp, d_state, stream=None) -> None:
+    _check(_lib().zero_adam_state_init(ctypes.byref(hp), _ptr(d_state), _stream(stream)),
+           "zero_adam_state_init")
+
+
+def zero_adam_state_advance(hp, d_state, stream=None) -> None:
+    _check(_lib().zero_adam_state_advance(ctypes.byref(hp), _ptr(d_state), _stream(stream)),
+           "zero_adam_state_advance")
 
 
 def zero_set_occupancy(kind: int, blocks_per_sm: int) -> int:

@@ -2,6 +2,7 @@
 // plan geometry and Adam constants to the kernels.  No call here allocates
 // device memory.
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <nvtx3/nvToolsExt.h>
@@ -86,21 +87,37 @@ zk::RankPtrs rank_ptrs(const zero_plan_t* p, const void* const* ptrs) {
 // by t successive fp64 multiplications (stopping once beta^t < 2^-60, when
 // 1 - beta^t is exactly 1 in fp64), subtracted from 1 in fp64, rounded once
 // to fp32.  (1 - beta) and lr*wd are fp32 operations.
-int adam_k(const zero_adam_t* hp, zk::AdamK* out) {
+// beta^t for both moments by t successive fp64 multiplications, each factor
+// stopping once below 2^-60 (where 1 - beta^t is exactly 1 in fp64).
+void beta_pows(float beta1, float beta2, int64_t step, double* p1, double* p2) {
+  double a = 1.0, b = 1.0;
+  const double b1 = (double)beta1, b2 = (double)beta2;
+  const double tiny = 8.673617379884035e-19;  // 2^-60
+  for (int64_t t = 0; t < step && (a >= tiny || b >= tiny); ++t) {
+    if (a >= tiny) a *= b1;
+    if (b >= tiny) b *= b2;
+  }
+  *p1 = a;
+  *p2 = b;
+}
+
+int check_hp(const zero_adam_t* hp) {
   if (!hp) return ZERO_EINVAL;
-  if (hp->step < 1) return ZERO_EINVAL;
   if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
     return ZERO_EINVAL;
   if (!isfinite(hp->lr) || !isfinite(hp->eps) || !isfinite(hp->weight_decay) ||
       !isfinite(hp->grad_scale))
     return ZERO_EINVAL;
+  if (hp->d_state && ((uintptr_t)hp->d_state & 7u) != 0) return ZERO_EALIGN;
+  return ZERO_OK;
+}
+
+int adam_k(const zero_adam_t* hp, zk::AdamK* out) {
+  int s = check_hp(hp);
+  if (s != ZERO_OK) return s;
+  if (!hp->d_state && hp->step < 1) return ZERO_EINVAL;
   double p1 = 1.0, p2 = 1.0;
-  const double b1 = (double)hp->beta1, b2 = (double)hp->beta2;
-  const double tiny = 8.673617379884035e-19;  // 2^-60
-  for (int64_t t = 0; t < hp->step && (p1 >= tiny || p2 >= tiny); ++t) {
-    if (p1 >= tiny) p1 *= b1;
-    if (p2 >= tiny) p2 *= b2;
-  }
+  if (!hp->d_state) beta_pows(hp->beta1, hp->beta2, hp->step, &p1, &p2);
   zk::AdamK k;
   k.lr = hp->lr;
   k.b1 = hp->beta1;
@@ -113,6 +130,9 @@ int adam_k(const zero_adam_t* hp, zk::AdamK* out) {
   k.lrwd = hp->lr * hp->weight_decay;
   k.has_wd = hp->weight_decay != 0.0f;
   k.scale = hp->grad_scale;
+  k.bcp = hp->d_state ? reinterpret_cast<const float*>(static_cast<const char*>(hp->d_state) +
+                                                       offsetof(zk::AdamState, bc1))
+                      : nullptr;
   *out = k;
   return ZERO_OK;
 }
@@ -319,4 +339,32 @@ extern "C" int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t m
   if (((uintptr_t)flag & 3u) != 0 || ((uintptr_t)d_status & 3u) != 0) return ZERO_EALIGN;
   return cuda_status(zk::launch_wait_flag(flag, expected, max_polls, d_status,
                                           (cudaStream_t)stream));
+}
+
+extern "C" int zero_adam_state_init(const zero_adam_t* hp, void* d_state, zero_stream_t stream) {
+  NvtxRange nvtx("zero_adam_state_init");
+  int s = check_hp(hp);
+  if (s != ZERO_OK) return s;
+  if (!d_state || hp->step < 1) return ZERO_EINVAL;
+  if (((uintptr_t)d_state & 7u) != 0) return ZERO_EALIGN;
+  zk::AdamState init{};
+  init.step = hp->step - 1;
+  beta_pows(hp->beta1, hp->beta2, init.step, &init.pow1, &init.pow2);
+  init.bc1 = (float)(1.0 - init.pow1);
+  init.bc2 = (float)(1.0 - init.pow2);
+  return cuda_status(zk::launch_adam_state(static_cast<zk::AdamState*>(d_state), &init,
+                                           (double)hp->beta1, (double)hp->beta2,
+                                           (cudaStream_t)stream));
+}
+
+extern "C" int zero_adam_state_advance(const zero_adam_t* hp, void* d_state,
+                                       zero_stream_t stream) {
+  NvtxRange nvtx("zero_adam_state_advance");
+  int s = check_hp(hp);
+  if (s != ZERO_OK) return s;
+  if (!d_state) return ZERO_EINVAL;
+  if (((uintptr_t)d_state & 7u) != 0) return ZERO_EALIGN;
+  return cuda_status(zk::launch_adam_state(static_cast<zk::AdamState*>(d_state), nullptr,
+                                           (double)hp->beta1, (double)hp->beta2,
+                                           (cudaStream_t)stream));
 }

@@ -44,7 +44,19 @@ struct GroupK {
 struct AdamK {
   float lr, b1, b2, omb1, omb2, eps, bc1, bc2, lrwd, scale;
   int has_wd;
+  const float* bcp;  // device {bc1, bc2} replacing bc1/bc2 when not null
 };
+
+// Device-resident Adam step state (ZERO_ADAM_STATE_BYTES).
+struct AdamState {
+  double pow1, pow2;  // beta1^t, beta2^t
+  int64_t step;       // t
+  float bc1, bc2;     // 1 - beta^t, rounded to fp32
+};
+static_assert(sizeof(AdamState) == ZERO_ADAM_STATE_BYTES, "device Adam state layout");
+
+cudaError_t launch_adam_state(AdamState* st, const AdamState* init, double b1, double b2,
+                              cudaStream_t s);
 
 enum OutMode : int { OUT_NONE = 0, OUT_FULL_BF16 = 1, OUT_FULL_F32 = 2, OUT_SHARDS_BF16 = 3 };
 

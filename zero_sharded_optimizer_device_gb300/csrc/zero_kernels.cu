@@ -33,6 +33,10 @@ __global__ void __launch_bounds__(kThreads)
                 const float* __restrict__ reduced, AdamK h, const float* __restrict__ coef_ptr,
                 int out_mode, void* __restrict__ out) {
   const float coef = coef_ptr ? *coef_ptr : 1.0f;
+  if (h.bcp) {  // bias corrections kept on the device (graph-replayable steps)
+    h.bc1 = h.bcp[0];
+    h.bc2 = h.bcp[1];
+  }
   const int64_t q0 = begin >> 3, q1 = (end + 7) >> 3;
   const bool flat_vec_ok = (g.flat_off & 7) == 0;
   for (int64_t q = q0 + gtid(); q < q1; q += gstride()) {
@@ -286,6 +290,35 @@ __global__ void wait_flag_kernel(const volatile uint32_t* flag, uint32_t expecte
 cudaError_t launch_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
                              int32_t* status, cudaStream_t st) {
   wait_flag_kernel<<<1, 1, 0, st>>>(flag, expected, max_polls, status);
+  return cudaGetLastError();
+}
+
+}  // namespace zk
+
+namespace zk {
+
+// ---------------------------------------------------------------------------
+// Device-resident Adam step: st <- init (when given), then one step on.
+// The same fp64 products and early stop as the host's computation.
+// ---------------------------------------------------------------------------
+__global__ void adam_state_kernel(AdamState* st, AdamState init, int has_init, double b1,
+                                  double b2) {
+  AdamState s = has_init ? init : *st;
+  if (!has_init) {
+    const double tiny = 8.673617379884035e-19;  // 2^-60
+    if (s.pow1 >= tiny) s.pow1 = __dmul_rn(s.pow1, b1);
+    if (s.pow2 >= tiny) s.pow2 = __dmul_rn(s.pow2, b2);
+    s.step += 1;
+    s.bc1 = __double2float_rn(__dsub_rn(1.0, s.pow1));
+    s.bc2 = __double2float_rn(__dsub_rn(1.0, s.pow2));
+  }
+  *st = s;
+}
+
+cudaError_t launch_adam_state(AdamState* st, const AdamState* init, double b1, double b2,
+                              cudaStream_t s) {
+  AdamState z{};
+  adam_state_kernel<<<1, 1, 0, s>>>(st, init ? *init : z, init ? 1 : 0, b1, b2);
   return cudaGetLastError();
 }
 

@@ -174,6 +174,10 @@ __global__ void __launch_bounds__(kThreads)
                  OutPtrs shards) {
   const int n = NT > 0 ? NT : g.n;
   const float coef = coef_ptr ? *coef_ptr : 1.0f;
+  if (h.bcp) {  // bias corrections kept on the device (graph-replayable steps)
+    h.bc1 = h.bcp[0];
+    h.bc2 = h.bcp[1];
+  }
   const int64_t q0 = begin >> 3, q1 = (end + 7) >> 3;
   const bool shard_vec_ok = ((g.rank_off | g.S) & 7) == 0;
   const bool flat_vec_ok = (g.flat_off & 7) == 0;  // 16-byte vectors in flat arrays
