@@ -209,7 +209,7 @@ def algorithmic_bytes(n_ranks: int, psi: int, grad_bytes: int) -> int:
 
 # --------------------------------------------------------- our GPU arm ----
 def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = False,
-                graph: bool = False) -> dict:
+                graph: bool = False, graph_steps: int = 1) -> dict:
     import torch
     import synth
     import zero_sharded_optimizer_device_gb300 as Z
@@ -244,8 +244,8 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
     torch.cuda.synchronize()
 
     if graph:
-        # one step captured once -- advance the device-resident Adam step
-        # state, then the fused kernel -- and replayed every step
+        # graph_steps steps captured once -- each: advance the device-resident
+        # Adam step state, then the fused kernel -- and replayed
         state = torch.zeros(4, dtype=torch.float64, device=dev)
         hp = Z.adam_hp(t[0] + 1, 1.0 / N, d_state=state)
         Z.zero_adam_state_init(hp, state, stream)
@@ -253,26 +253,29 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
+        per = max(1, min(graph_steps, steps))
         with torch.cuda.stream(side), torch.cuda.graph(g, stream=side):
-            Z.zero_adam_state_advance(hp, state, side)
-            Z.zero_step(plan, 0, grads, zg, master, m, v, hp, None, out, Z.ZERO_BF16, side)
+            for _ in range(per):
+                Z.zero_adam_state_advance(hp, state, side)
+                Z.zero_step(plan, 0, grads, zg, master, m, v, hp, None, out, Z.ZERO_BF16, side)
         stream.wait_stream(side)
         for _ in range(3):
             g.replay()
+        reps = max(1, steps // per)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(dev.index) as clocks:
             dist.barrier()
             torch.cuda.synchronize()
             t0.record(stream)
-            for _ in range(steps):
+            for _ in range(reps):
                 g.replay()
             t1.record(stream)
             torch.cuda.synchronize()
             dist.barrier()
-        ms = t0.elapsed_time(t1) / steps
+        ms = t0.elapsed_time(t1) / (reps * per)
         return dict(local_ms=ms, launch_ms=ms, e2e_ms=None, psi=w.psi, psi_pad=P, n_ranks=N,
                     gbytes=gbytes, copy_gbs=None, clocks=clocks.summary(), h2d=0, d2h=0,
-                    e2e_steps=0, e2e_transfer="not measured with --graph", graph=True)
+                    e2e_steps=0, e2e_transfer="not measured with --graph", graph=per)
 
     if kernel_only:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -733,6 +736,8 @@ def main(argv=None):
                     help="time only the step kernel: no copy peak, e2e or CPU baseline")
     ap.add_argument("--graph", action="store_true",
                     help="replay one CUDA-graph-captured step (device-resident Adam step state)")
+    ap.add_argument("--graph-steps", type=int, default=1,
+                    help="with --graph: steps captured in one graph (amortises the replay launch)")
     ap.add_argument("--grad-dtype", choices=["bf16", "f32"], default=None,
                     help="override the workload's gradient dtype (fp32 doubles the source bytes)")
     ap.add_argument("--gather-sweep", action="store_true",
@@ -793,7 +798,8 @@ def main(argv=None):
         dist.close()
         return
 
-    res = bench_fused(w, args.steps, args.warmup, dist, args.kernel_only, args.graph)
+    res = bench_fused(w, args.steps, args.warmup, dist, args.kernel_only, args.graph,
+                      args.graph_steps)
     ms = dist.max(res["local_ms"])
     e2e_ms = dist.max(res["e2e_ms"]) if res["e2e_ms"] is not None else None
     n_gpus = dist.world
@@ -828,7 +834,8 @@ def main(argv=None):
         "gpu_launches": 2 * args.steps if res.get("graph") else args.steps,
     }
     if res.get("graph"):
-        line["config"]["launch"] = "one CUDA graph per step: Adam state advance + fused kernel"
+        line["config"]["launch"] = (f"CUDA graph of {res['graph']} step(s), each an Adam state "
+                                    "advance + the fused kernel")
     if args.kernel_only:
         line = {"kernel_only": True, "workload": w.name, "psi": w.psi, "ms_per_step": ms,
                 "value": value, "unit": "Gparams/s", "roofline": line["roofline"]}

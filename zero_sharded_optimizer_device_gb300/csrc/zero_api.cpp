@@ -83,12 +83,10 @@ zk::RankPtrs rank_ptrs(const zero_plan_t* p, const void* const* ptrs) {
   return r;
 }
 
-// Adam constants.  The bias corrections 1 - beta^t: beta (fp32) raised to t
-// by t successive fp64 multiplications (stopping once beta^t < 2^-60, when
-// 1 - beta^t is exactly 1 in fp64), subtracted from 1 in fp64, rounded once
-// to fp32.  (1 - beta) and lr*wd are fp32 operations.
-// beta^t for both moments by t successive fp64 multiplications, each factor
-// stopping once below 2^-60 (where 1 - beta^t is exactly 1 in fp64).
+// beta^t for both moments: the fp32 beta raised to t by t successive fp64
+// multiplications, each factor stopping once below 2^-60 (where 1 - beta^t
+// is exactly 1 in fp64).  The bias corrections are 1 - beta^t in fp64,
+// rounded once to fp32; (1 - beta) and lr*wd are fp32 operations.
 void beta_pows(float beta1, float beta2, int64_t step, double* p1, double* p2) {
   double a = 1.0, b = 1.0;
   const double b1 = (double)beta1, b2 = (double)beta2;
