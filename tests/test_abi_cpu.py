@@ -191,3 +191,24 @@ def test_set_occupancy_round_trip_and_limits():
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_set_occupancy(kind, n)
         assert e.value.status == Z.ZERO_EINVAL
+
+
+def test_header_compiles_as_c99_and_library_links(tmp_path):
+    """A plain C99 program includes include/zero.h, links libzero.so and
+    plans the tiny workload on the CPU."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    lib_dir = os.path.join(root, "zero_sharded_optimizer_device_gb300")
+    exe = str(tmp_path / "c_abi_check")
+    cc = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                         "-I", os.path.join(root, "include"),
+                         os.path.join(root, "tests", "c_abi_check.c"),
+                         "-L", lib_dir, "-lzero", f"-Wl,-rpath,{lib_dir}", "-o", exe],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    out = subprocess.run([exe], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    lines = out.stdout.splitlines()
+    assert lines[0] == "psi 10000 psi_pad 10048 shard 2512"
+    assert lines[2] == "rank 1: (0 2512 2512 1584) (1 0 4096 928)"
+    assert lines[5] == "stage2 17584 55264 volume 7536 7536"
+    assert lines[6] == f"bad {Z.ZERO_EINVAL} invalid argument"
