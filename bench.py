@@ -577,7 +577,7 @@ def regroup(w, per: str):
     return [g // k for g in w.groups]
 
 
-def bench_gather_sweep(w, steps: int, dist: Dist) -> dict:
+def bench_gather_sweep(w, steps: int, dist: Dist, only=None) -> dict:
     """Forward + reverse per-group gathers of the stage-3 workload's bf16
     shards at several partition granularities (the shards are generated
     directly; no optimizer step is needed to time the gathers)."""
@@ -591,6 +591,8 @@ def bench_gather_sweep(w, steps: int, dist: Dist) -> dict:
     sa = torch.cuda.current_stream(dev)
     res = {}
     for per in ("tensor", "layer", "2-layers", "4-layers"):
+        if only and per != only:
+            continue
         groups_of = regroup(w, per)
         plan = Z.zero_plan(w.numels, N, w.align, groups_of)
         info = Z.zero_plan_info(plan)
@@ -742,6 +744,9 @@ def main(argv=None):
                     help="override the workload's gradient dtype (fp32 doubles the source bytes)")
     ap.add_argument("--gather-sweep", action="store_true",
                     help="stage-3 workload: gather bandwidth at several partition granularities")
+    ap.add_argument("--gather-granularity", default=None,
+                    choices=["tensor", "layer", "2-layers", "4-layers"],
+                    help="with --gather-sweep: only this granularity")
     args = ap.parse_args(argv)
     from synth import workloads as W
     w = W.ALL[args.workload]
@@ -785,7 +790,7 @@ def main(argv=None):
     import zero_sharded_optimizer_device_gb300  # noqa: F401  (fails loudly when unbuilt)
 
     if args.gather_sweep:
-        res = bench_gather_sweep(w, max(1, args.steps), dist)
+        res = bench_gather_sweep(w, max(1, args.steps), dist, args.gather_granularity)
         if dist.rank == 0:
             print(json.dumps({"workload": f"{w.name} stage-3 gathers, forward + reverse",
                               "n_ranks": w.n_ranks, "granularity": res}), flush=True)
