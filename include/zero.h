@@ -140,7 +140,8 @@ int zero_last_cuda_error(void);
  * [r*S_g, (r+1)*S_g).  group_of_tensor (may be NULL = one group) gives each
  * tensor's layer group; it must start at 0 and be non-decreasing without
  * gaps (stage 3 plans every layer group on its own [P4 "Implementation
- * Strategy"]).  numels[t] >= 0; 1 <= N <= 64; align >= 1.
+ * Strategy"]).  numels[t] >= 0; 1 <= N <= 64; align >= 1; every group's
+ * psi_pad below 2^40 elements (the kernels' index range).
  * Errors: ZERO_EINVAL (bad arguments or group list, size overflow),
  * ZERO_ENOMEM.  *out is set only on success. */
 int zero_plan(const int64_t* numels, int64_t n_tensors, int32_t n_ranks, int32_t align,

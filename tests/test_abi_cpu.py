@@ -76,6 +76,10 @@ def test_plan_argument_errors():
     with pytest.raises(Z.ZeroError) as e:
         Z.zero_plan([2 ** 62, 2 ** 62], 2, 1)
     assert e.value.status == Z.ZERO_EINVAL
+    with pytest.raises(Z.ZeroError) as e:          # a group at the kernels' 2^40 index limit
+        Z.zero_plan([1 << 40], 4, 1)
+    assert e.value.status == Z.ZERO_EINVAL
+    Z.zero_plan([(1 << 40) - 64], 4, 16)          # just below it is fine
     p = Z.zero_plan([10], 2, 1)
     for f, a in [(Z.zero_plan_group, (1,)), (Z.zero_plan_shard, (0, 2)),
                  (Z.zero_plan_tensor, (1,)), (Z.zero_plan_memory, (4,))]:

@@ -72,7 +72,7 @@ zk::GroupK group_k(const zero_plan_t* p, int32_t group) {
   k.S = g.shard;
   k.flat_off = g.flat_off;
   k.rank_off = g.rank_off;
-  k.invS = g.shard > 0 ? 1.0f / (float)g.shard : 0.0f;
+  k.invS256 = g.shard > 0 ? 256.0f / (float)g.shard : 0.0f;
   k.n = p->n_ranks;
   return k;
 }

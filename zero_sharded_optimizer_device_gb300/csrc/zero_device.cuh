@@ -104,10 +104,12 @@ struct GradVec<float> {
   }
 };
 
-// Owner rank of group-local element i: floor(i / S), found from a float
-// estimate and corrected with exact integer compares.
+// Owner rank of group-local element i: floor(i / S), found from an fp32
+// estimate and corrected with exact integer compares.  The estimate converts
+// i/256 as a 32-bit integer (i < 2^40): a 64-bit integer conversion would run
+// on the FP64 pipe, which is narrow on this GPU.
 __device__ __forceinline__ int owner_of(int64_t i, const GroupK& g) {
-  int k = __float2int_rz(__ll2float_rz(i) * g.invS);
+  int k = __float2int_rz(__uint2float_rz((uint32_t)(i >> 8)) * g.invS256);
   k = k < 0 ? 0 : (k > g.n - 1 ? g.n - 1 : k);
   while (k > 0 && (int64_t)k * g.S > i) --k;
   while (k < g.n - 1 && (int64_t)(k + 1) * g.S <= i) ++k;

@@ -36,7 +36,7 @@ struct GroupK {
   int64_t S;         // shard size
   int64_t flat_off;  // group start in flat arrays
   int64_t rank_off;  // group start in per-rank shard buffers
-  float invS;        // ~1/S, refined with integer checks
+  float invS256;     // ~256/S, for the owner estimate (refined with integer checks)
   int n;             // ranks
 };
 

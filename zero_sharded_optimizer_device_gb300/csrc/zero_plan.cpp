@@ -71,6 +71,7 @@ extern "C" int zero_plan(const int64_t* numels, int64_t n_tensors, int32_t n_ran
       if (blocks > std::numeric_limits<int64_t>::max() / quantum) { delete p; return ZERO_EINVAL; }
       gi.psi = psi;
       gi.psi_pad = blocks * quantum;
+      if (gi.psi_pad >= (int64_t(1) << 40)) { delete p; return ZERO_EINVAL; }  // kernel index range
       gi.shard = gi.psi_pad / n_ranks;
       gi.flat_off = flat;
       gi.rank_off = rank_off;

@@ -65,7 +65,7 @@ extern "C" int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* o
     k.S = gi.shard;
     k.flat_off = gi.flat_off;
     k.rank_off = gi.rank_off;
-    k.invS = gi.shard > 0 ? 1.0f / (float)gi.shard : 0.0f;
+    k.invS256 = gi.shard > 0 ? 256.0f / (float)gi.shard : 0.0f;
     k.n = plan->n_ranks;
     return k;
   };
