@@ -342,3 +342,39 @@ def test_cuda_graph_of_the_bucketed_clip_pipeline(cuda):
     torch.cuda.synchronize()
     assert torch.equal(a.master, b.master) and torch.equal(a.m, b.m) and torch.equal(a.v, b.v)
     assert torch.equal(ba[3], bb[3]) and torch.equal(ba[2], bb[2])
+
+
+def test_fp32_gradient_load_paths_agree(cuda):
+    """fp32 gradient buffers that are all 32-byte aligned take one 32-byte
+    load per thread, others two 16-byte loads: identical results, device and
+    mapped pinned host memory alike."""
+    import torch
+    import bench
+    c = Case([40_000, 1_234], 8, 16, "f32", grad_sigma=1e-2, seed=61, host_state=False)
+    Z = c.Z
+    P = c.info["psi_pad"]
+    aligned = c.grads_dev(0, 1)
+    offset = []                                   # same values at a 16-byte (not 32) offset
+    for g in aligned:
+        buf = torch.empty(P + 4, dtype=torch.float32, device=cuda)
+        buf[4:].copy_(g)
+        assert (buf[4:].data_ptr() % 32) == 16
+        offset.append(buf[4:])
+    results = []
+    for grads in (aligned, offset):
+        master, m, v = c.master.clone(), c.m.clone(), c.v.clone()
+        out = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+        Z.zero_step(c.plan, 0, grads, Z.ZERO_F32, master, m, v, c.hp_dev(1), None, out)
+        results.append((master, m, v, out))
+    h = [torch.empty(P, dtype=torch.float32, pin_memory=True) for _ in range(8)]
+    for x, g in zip(h, aligned):
+        x.copy_(g)
+    if all(bench.host_mapped(x) for x in h):
+        master, m, v = c.master.clone(), c.m.clone(), c.v.clone()
+        out = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+        Z.zero_step(c.plan, 0, h, Z.ZERO_F32, master, m, v, c.hp_dev(1), None, out)
+        results.append((master, m, v, out))
+    torch.cuda.synchronize()
+    for r in results[1:]:
+        for a, b in zip(r, results[0]):
+            assert torch.equal(a, b)

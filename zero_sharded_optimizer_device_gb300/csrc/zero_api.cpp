@@ -77,6 +77,15 @@ zk::GroupK group_k(const zero_plan_t* p, int32_t group) {
   return k;
 }
 
+// fp32 gradients with every buffer 32-byte aligned take the fused kernel's
+// one-load-per-thread variant.
+int fused_gdtype(const zero_plan_t* p, int gdtype, const void* const* grads) {
+  if (gdtype != ZERO_F32) return gdtype;
+  for (int r = 0; r < p->n_ranks; ++r)
+    if ((uintptr_t)grads[r] & 31u) return gdtype;
+  return zk::kF32Aligned32;
+}
+
 zk::RankPtrs rank_ptrs(const zero_plan_t* p, const void* const* ptrs) {
   zk::RankPtrs r{};
   for (int i = 0; i < p->n_ranks; ++i) r.p[i] = ptrs[i];
@@ -273,7 +282,7 @@ extern "C" int zero_step(const zero_plan_t* plan, int32_t group, const void* con
   const int mode = !full_out ? zk::OUT_NONE
                              : (out_dtype == ZERO_BF16 ? zk::OUT_FULL_BF16 : zk::OUT_FULL_F32);
   zk::OutPtrs none{};
-  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), gdtype, group_k(plan, group), 0,
+  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), fused_gdtype(plan, gdtype, grads), group_k(plan, group), 0,
                                       plan->groups[group].psi_pad, master, m, v, k, d_coef, mode,
                                       full_out, none, (cudaStream_t)stream));
 }
@@ -295,7 +304,7 @@ extern "C" int zero_step_group(const zero_plan_t* plan, int32_t group, const voi
   ZERO_TRY(adam_k(hp, &k));
   zk::OutPtrs out{};
   for (int r = 0; r < plan->n_ranks; ++r) out.p[r] = shards[r];
-  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), gdtype, group_k(plan, group), 0,
+  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), fused_gdtype(plan, gdtype, grads), group_k(plan, group), 0,
                                       plan->groups[group].psi_pad, master, m, v, k, d_coef,
                                       zk::OUT_SHARDS_BF16, nullptr, out, (cudaStream_t)stream));
 }

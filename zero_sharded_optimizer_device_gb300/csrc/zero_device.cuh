@@ -104,6 +104,31 @@ struct GradVec<float> {
   }
 };
 
+// fp32 gradients whose buffers are 32-byte aligned: the 8 values of a thread
+// in one 32-byte load, so that a warp's load covers 1 KiB without gaps (two
+// 16-byte loads per thread leave every other 16 bytes to the second load,
+// which host memory read over the link serves at half rate).
+struct F32x8 {};
+
+template <>
+struct GradVec<F32x8> {
+  float r[8];
+  __device__ __forceinline__ void load(const void* base, int64_t i) {
+    const float* p = static_cast<const float*>(base) + i;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]),
+                   "=f"(r[6]), "=f"(r[7])
+                 : "l"(p));
+  }
+  __device__ __forceinline__ void get(float f[8]) const {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = r[e];
+  }
+  __device__ __forceinline__ static float load1(const void* base, int64_t i) {
+    return static_cast<const float*>(base)[i];
+  }
+};
+
 // Owner rank of group-local element i: floor(i / S), found from an fp32
 // estimate and corrected with exact integer compares.  The estimate converts
 // i/256 as a 32-bit integer (i < 2^40): a 64-bit integer conversion would run

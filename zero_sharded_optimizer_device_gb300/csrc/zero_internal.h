@@ -58,6 +58,9 @@ static_assert(sizeof(AdamState) == ZERO_ADAM_STATE_BYTES, "device Adam state lay
 cudaError_t launch_adam_state(AdamState* st, const AdamState* init, double b1, double b2,
                               cudaStream_t s);
 
+// launch_fused only: fp32 gradients whose N buffers are all 32-byte aligned.
+constexpr int kF32Aligned32 = 2;
+
 enum OutMode : int { OUT_NONE = 0, OUT_FULL_BF16 = 1, OUT_FULL_F32 = 2, OUT_SHARDS_BF16 = 3 };
 
 // What the reduce-scatter does with the ring sum of each element.

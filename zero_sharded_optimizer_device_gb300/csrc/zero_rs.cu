@@ -272,6 +272,20 @@ cudaError_t dispatch(int n, int gdtype, A&&... a) {
   }
 }
 
+// The fused step only: fp32 sources that are all 32-byte aligned.
+template <template <int, typename> class Launch, typename... A>
+cudaError_t dispatch_f32_wide(int n, A&&... a) {
+  switch (n) {
+    case 2: return Launch<2, F32x8>::run(a...);
+    case 4: return Launch<4, F32x8>::run(a...);
+    case 8: return Launch<8, F32x8>::run(a...);
+    case 16: return Launch<16, F32x8>::run(a...);
+    case 32: return Launch<32, F32x8>::run(a...);
+    case 64: return Launch<64, F32x8>::run(a...);
+    default: return Launch<0, F32x8>::run(a...);
+  }
+}
+
 template <int NT, typename GT>
 struct RsLaunch {
   // One grid for a window of n elements: one block per 256 vectors, at most
@@ -337,6 +351,9 @@ cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64
                          const float* coef, int out_mode, void* out_full,
                          const OutPtrs& shards, cudaStream_t st) {
   if (end <= begin) return cudaSuccess;
+  if (gdtype == kF32Aligned32)
+    return dispatch_f32_wide<FusedLaunch>(g.n, src, g, begin, end, master, m, v, h, coef,
+                                          out_mode, out_full, shards, st);
   return dispatch<FusedLaunch>(g.n, gdtype, src, g, begin, end, master, m, v, h, coef,
                                out_mode, out_full, shards, st);
 }
