@@ -183,9 +183,14 @@ __global__ void __launch_bounds__(kThreads)
   const bool vec_ok = ((g.S | g.rank_off) % VW) == 0;
   if (vec_ok) {
     const int64_t nv = psi_pad / VW;  // psi_pad is a multiple of S, so of VW
+    int k = 0;                        // a thread's indices only grow: track the owner
+    int64_t next = g.S;               // first element of owner k + 1
     for (int64_t q = gtid(); q < nv; q += gstride()) {
       const int64_t j = q * VW;
-      const int k = owner_of(j, g);
+      while (j >= next) {
+        ++k;
+        next += g.S;
+      }
       const char* s = static_cast<const char*>(shards.p[k]) +
                       (g.rank_off + (j - (int64_t)k * g.S)) * ES;
       st_stream(static_cast<char*>(out) + j * ES, ld_once(s));
