@@ -677,6 +677,17 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
+def fused_config(w, n_gpus: int) -> dict:
+    """The `config` object both arms report for a fused-step workload."""
+    abytes = algorithmic_bytes(w.n_ranks, w.psi, 2 if w.grad_dtype == "bf16" else 4)
+    return {"workload": f"{w.name} fused zero_step", "psi": w.psi, "n_ranks": w.n_ranks,
+            "align": w.align, "grad_dtype": w.grad_dtype, "state": "fp32 master/m/v",
+            "gathered": "bf16",
+            "parallelism": f"replicas x{n_gpus} (ranks emulated on each GPU)",
+            "bytes_per_step": abytes,
+            "l2": f"inputs {abytes / 1e9:.2f} GB per step > L2 129 MB, no flush"}
+
+
 def secondary_line(w, args, dist) -> dict:
     """JSON line for the bucketed and stage-3 workloads (not the headline)."""
     peak, peak_kind = measured_hbm_peak()
@@ -775,8 +786,7 @@ def main(argv=None):
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": el / steps * 1e3, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": f"{w.name} fused ZeRO step (oracle window)",
-                           "psi": w.psi, "n_ranks": w.n_ranks, "sample_params": win},
+                "config": fused_config(w, args.gpus),
                 "cpu_baseline": {"value": value, "unit": "Gparams/s", "cores": 1,
                                  "kind": "oracle", "sample": desc, "cpu": cpu_model()},
                 "e2e": {"value": value, "unit": "Gparams/s", "h2d_bytes_per_step": 0,
@@ -819,12 +829,7 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{w.name} fused zero_step", "psi": w.psi,
-                   "n_ranks": res["n_ranks"], "align": w.align, "grad_dtype": w.grad_dtype,
-                   "state": "fp32 master/m/v", "gathered": "bf16",
-                   "parallelism": f"replicas x{n_gpus} (ranks emulated on each GPU)",
-                   "bytes_per_step": abytes,
-                   "l2": f"inputs {abytes / 1e9:.2f} GB per step > L2 129 MB, no flush"},
+        "config": fused_config(w, n_gpus),
         "hbm_gbs": step_gbs, "hbm_pct_of_peak": 100.0 * step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
