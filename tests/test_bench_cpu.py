@@ -1,0 +1,54 @@
+"""The benchmark's JSON contract and helpers, on the CPU: the reference arm
+(the oracle on a bounded window) prints one line with the required keys, and
+the clock sampler parses nvidia-smi rows and reports throttle reasons."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+from synth import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_the_contract_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "1"], capture_output=True, text=True,
+                         timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [x for x in out.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e", "impl"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["config"] == bench.fused_config(W.GPT2_SMALL, 1)
+
+
+def test_clock_sampler_parses_rows_and_reasons():
+    cs = bench.ClockSampler(0)
+    cs.out = "\n".join([
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2070, 2070, 1300.5, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 345, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2040, 2070, 1350.0, 0x0, Not Active, Not Active, Active, Not Active",
+    ])
+    s = cs.summary()
+    assert s["sm_max_mhz"] == 2070.0 and s["samples"] == 4
+    assert s["sm_mhz"] == 2070.0                    # idle samples (< half the top) are ignored
+    assert s["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
+    cs.out = ""
+    assert cs.summary()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_algorithmic_bytes_formula():
+    # N sources of the gradient dtype + 12 B state read + 12 B written + 2 B bf16 out
+    assert bench.algorithmic_bytes(8, 124_439_808, 2) == 124_439_808 * 42
+    assert bench.algorithmic_bytes(64, 10, 2) == 10 * 154
+    assert bench.algorithmic_bytes(8, 10, 4) == 10 * 58
