@@ -467,13 +467,14 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist) -> dict:
 
 
 # ------------------------------------------- stage 3: step + per-layer gathers --
-def bench_stage3(w, steps: int, warmup: int, dist: Dist) -> dict:
+def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False) -> dict:
     """Stage 3 (the Llama-7B workload): per layer group, in reverse order, a
     fused reduce-scatter + Adam writing each owner's bf16 shard (gradients
     regenerated into one slot per group, untimed); then every group gathered
     into a contiguous layer buffer in forward and then reverse order, the
     next group prefetched on a second stream while a consumer reads the
-    current one."""
+    current one.  With ``use_graph`` the gather pass is also captured once in
+    a CUDA graph and its replay timed."""
     import torch
     import synth
     import zero_sharded_optimizer_device_gb300 as Z
@@ -548,18 +549,42 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist) -> dict:
     for s in range(1, warmup + 1):
         rs_adam_step(s)
         gather_schedule()
-    rs_ms, sched_ms, gonly_ms, bcast_ms = [], [], [], []
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        gs, gsb = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        gs.wait_stream(sa)
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(graph, stream=gs):
+                Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, gs, gsb)
+        sa.wait_stream(gs)
+        torch.cuda.synchronize()
+
+    def gather_schedule_graph():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(sa)
+        graph.replay()
+        e1.record(sa)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    if graph is not None:
+        gather_schedule_graph()
+    rs_ms, sched_ms, gonly_ms, bcast_ms, graph_ms = [], [], [], [], []
     with ClockSampler(dev.index) as clocks:
         dist.barrier()
         for s in range(warmup + 1, warmup + steps + 1):
             rs_ms.append(rs_adam_step(s))
             sched_ms.append(gather_schedule())
+            if graph is not None:
+                graph_ms.append(gather_schedule_graph())
             gonly_ms.append(gathers_only())
             bcast_ms.append(broadcasts_only())
         dist.barrier()
     gather_elems = 2 * sum(g["psi_pad"] for g in groups)
     return dict(rs_ms=statistics.fmean(rs_ms), sched_ms=statistics.fmean(sched_ms),
                 gonly_ms=statistics.fmean(gonly_ms), bcast_ms=statistics.fmean(bcast_ms),
+                graph_ms=statistics.fmean(graph_ms) if graph_ms else None,
                 P=P, N=N, groups=len(groups),
                 gather_elems=gather_elems, clocks=clocks.summary())
 
@@ -713,7 +738,7 @@ def secondary_line(w, args, dist) -> dict:
                              "rs_ms": r["rs_ms"], "adam_ms": r["adam_ms"], "norm_ms": r["norm_ms"]},
                 "norm": r["norm"], "clip_coef": r["coef"], "clocks": r["clocks"],
                 "gpu_launches": r["n_launches"] * args.steps}
-    r = bench_stage3(w, args.steps, args.warmup, dist)
+    r = bench_stage3(w, args.steps, args.warmup, dist, args.graph)
     P, N = r["P"], r["N"]
     rs_ms = dist.max(r["rs_ms"])
     return {"metric": METRIC, "value": n_gpus * w.psi / (rs_ms * 1e-3) / 1e9,
@@ -729,7 +754,10 @@ def secondary_line(w, args, dist) -> dict:
                        "broadcast_ms": r["bcast_ms"],
                        "broadcast_gbs": 4 * r["gather_elems"] / (r["bcast_ms"] * 1e-3) / 1e9,
                        "schedule_gbs_incl_consumer": 6 * r["gather_elems"] /
-                       (r["sched_ms"] * 1e-3) / 1e9},
+                       (r["sched_ms"] * 1e-3) / 1e9,
+                       **({"schedule_graph_ms": r["graph_ms"],
+                           "schedule_graph_gbs_incl_consumer": 6 * r["gather_elems"] /
+                           (r["graph_ms"] * 1e-3) / 1e9} if r["graph_ms"] else {})},
             "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind},
             "clocks": r["clocks"]}
 
@@ -748,7 +776,8 @@ def main(argv=None):
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the step kernel: no copy peak, e2e or CPU baseline")
     ap.add_argument("--graph", action="store_true",
-                    help="replay one CUDA-graph-captured step (device-resident Adam step state)")
+                    help="replay one CUDA-graph-captured step (device-resident Adam step state); "
+                         "stage-3 workload: also time the gather pass replayed from a graph")
     ap.add_argument("--graph-steps", type=int, default=1,
                     help="with --graph: steps captured in one graph (amortises the replay launch)")
     ap.add_argument("--grad-dtype", choices=["bf16", "f32"], default=None,

@@ -223,6 +223,46 @@ def test_native_gather_schedule_matches_direct_gathers(cuda):
         assert e.value.status == status
 
 
+def test_cuda_graph_of_the_stage3_gather_pass(cuda):
+    """The two-stream gather schedule captured once in a CUDA graph (stream B
+    forks from and joins the capturing stream through the pass's events);
+    a replay after the shards changed gives the eager pass's checksums."""
+    import torch
+    d, ffn, vocab = 64, 172, 500
+    blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(3)]
+    numels = [vocab * d] + [n for b in blocks for n in b] + [d, vocab * d]
+    groups = [0] + [1 + i // 9 for i in range(27)] + [4, 4]
+    c = Case(numels, 16, 16, "bf16", seed=6, groups=groups, host_state=False)
+    Z = c.Z
+    N, G = 16, len(c.groups)
+    shards = [torch.randn(c.info["shard_total"], device=cuda).to(torch.bfloat16)
+              for _ in range(N)]
+    gmax = max(g["psi_pad"] for g in c.groups)
+    bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=cuda) for _ in range(2)]
+    order = list(range(G)) + list(reversed(range(G)))
+    eager = torch.zeros(len(order), dtype=torch.int64, device=cuda)
+    replayed = torch.zeros(len(order), dtype=torch.int64, device=cuda)
+    cur = torch.cuda.current_stream()
+    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, eager, cur, torch.cuda.Stream())
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    s.wait_stream(cur)
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, replayed, s, sb)
+    cur.wait_stream(s)
+    torch.cuda.synchronize()
+    for r in range(N):
+        shards[r].copy_(torch.randn(c.info["shard_total"], device=cuda).to(torch.bfloat16))
+    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, eager, cur, torch.cuda.Stream())
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager, replayed)
+    assert int(torch.count_nonzero(eager)) == len(order)
+
+
 def _eager_and_state_cases(w, seed):
     a = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, seed,
              host_state=False)
