@@ -285,8 +285,10 @@ int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const*
  * for the work already queued on stream A; work queued on stream A after the
  * call runs after every gather and consumer.  layer_bufs: 2 device buffers
  * of buf_elems bf16 elements each (>= psi_pad of every group in order);
- * d_sums: n uint64.  stream_a != stream_b.  Uses four CUDA events created
- * and released inside the call; allocates no device memory.
+ * d_sums: n uint64.  stream_a != stream_b.  Uses five CUDA events created
+ * and released inside the call; allocates no device memory.  The call may be
+ * captured in a CUDA graph: with stream_a capturing, stream_b joins the
+ * capture through those events and rejoins stream_a before the call returns.
  * Errors: EINVAL, EALIGN, ERANGE (group id or buffer size), ECUDA. */
 int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* order, int32_t n,
                             const void* const* shards, void* const* layer_bufs,
