@@ -363,6 +363,52 @@ int zero_set_occupancy(int32_t kind, int32_t blocks_per_sm, int32_t* previous);
  * 16-byte loads and stores; measures the achievable HBM copy bandwidth. */
 int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_t stream);
 
+/* ------------------------------------------------------ checked build --
+ * No counterpart on the pages: a stand-in for a device memory checker.  The
+ * library built with -DZERO_CHECKED (libzero_checked.so, same ABI) tests
+ * every global access of its kernels against the extent this header gives
+ * the buffer: a gradient buffer's [0, psi_pad(g)), the call's window of a
+ * flat array, owner k's chunk [k*S_g, (k+1)*S_g) of a group, a shard
+ * buffer's [rank_off(g), rank_off(g) + S_g), a layer buffer's [0, psi_pad(g)),
+ * a partial-sum array's [0, n).  An access outside is skipped (never made)
+ * and counted; the first one is recorded with its site and extent.  The
+ * release library has no checks and reports checked = 0, count = 0. */
+#define ZERO_SITE_PROBE 1        /* zero_bounds_probe */
+#define ZERO_SITE_RS_GRAD 2      /* reduce-scatter: gradient buffers */
+#define ZERO_SITE_RS_FLAT 3      /* reduce-scatter: reduced window */
+#define ZERO_SITE_RS_OWNER 4     /* reduce-scatter: owner chunk */
+#define ZERO_SITE_STEP_GRAD 5    /* fused step: gradient buffers */
+#define ZERO_SITE_STEP_FLAT 6    /* fused step: master, m, v, full output window */
+#define ZERO_SITE_STEP_OWNER 7   /* fused step: owner chunk */
+#define ZERO_SITE_STEP_SHARD 8   /* fused step: owner's shard buffer */
+#define ZERO_SITE_ADAM_FLAT 9    /* Adam: reduced, master, m, v, output window */
+#define ZERO_SITE_CAST_FLAT 10   /* all-gather cast window */
+#define ZERO_SITE_NORM 11        /* norm: partial sums */
+#define ZERO_SITE_GATHER_SHARD 12 /* stage-3 gather: source shard */
+#define ZERO_SITE_GATHER_OUT 13  /* stage-3 gather: layer buffer */
+#define ZERO_SITE_CHECKSUM 14    /* layer checksum: layer buffer */
+#define ZERO_SITE_COPY 15        /* zero_copy */
+
+typedef struct {
+  int32_t checked; /* 1 in the checked build */
+  int32_t site;    /* ZERO_SITE_* of the first access outside its extent; 0 if none */
+  int64_t count;   /* accesses outside their extent since the last reset */
+  int64_t index;   /* first one: start of the accessed element range */
+  int64_t lo, hi;  /* first one: the extent [lo, hi) it broke */
+} zero_bounds_t;
+
+/* zero_bounds_report: synchronizes the current device, then copies the
+ * record of the kernels run on it to *out; reset != 0 clears the record
+ * afterwards.  Release build: fills checked = 0 and zeros, touches no device.
+ * Errors: EINVAL (out NULL), ECUDA. */
+int zero_bounds_report(zero_bounds_t* out, int32_t reset);
+
+/* zero_bounds_probe: checked build only (a no-op returning ZERO_OK in the
+ * release build): a one-thread kernel that makes no memory access and
+ * records one out-of-extent access at ZERO_SITE_PROBE (index 1, extent
+ * [0, 1)), so a caller can confirm the record reaches the host. */
+int zero_bounds_probe(zero_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,3 +33,19 @@ def cuda():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _no_out_of_extent_access(request):
+    """Under the bounds-checked library (ZERO_CHECKED=1), every GPU test must
+    leave the kernels' out-of-extent record empty."""
+    yield
+    if os.environ.get("ZERO_CHECKED") != "1" or request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+    if not torch.cuda.is_available():
+        return
+    import zero_sharded_optimizer_device_gb300 as Z
+    r = Z.zero_bounds_report(reset=True)
+    assert r["checked"] == 1, "ZERO_CHECKED=1 but the release library is loaded"
+    assert r["count"] == 0, f"kernel accesses outside their buffer's extent: {r}"

@@ -25,6 +25,28 @@ def test_library_exports_every_declared_function():
         assert callable(getattr(Z, name)), name
 
 
+def test_checked_build_exports_the_same_functions():
+    import ctypes
+    path = os.path.join(os.path.dirname(Z.binding.LIB_PATH), "libzero_checked.so")
+    if not os.path.exists(path):
+        pytest.skip("libzero_checked.so not built")
+    lib = ctypes.CDLL(path)
+    for name in Z.header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_release_bounds_report_is_empty_without_a_device():
+    """The release library has no checks: its report needs no device and says
+    so; its probe is a no-op."""
+    if os.environ.get("ZERO_CHECKED") == "1":
+        pytest.skip("checked build loaded")
+    assert Z.zero_bounds_report() == dict(checked=0, site=0, count=0, index=0, lo=0, hi=0)
+    Z.zero_bounds_probe(0)
+    with pytest.raises(Z.ZeroError) as e:
+        Z.binding._check(Z.binding._lib().zero_bounds_report(None, 0), "zero_bounds_report")
+    assert e.value.status == Z.ZERO_EINVAL
+
+
 def test_strerror_covers_every_status():
     for code in range(0, -8, -1):
         assert Z.zero_strerror(code) and Z.zero_strerror(code) != "unknown status"

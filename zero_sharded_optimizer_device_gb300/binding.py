@@ -14,7 +14,10 @@ import os
 import re
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libzero.so")
+# ZERO_CHECKED=1 in the environment loads the bounds-checked build of the same
+# ABI instead (every kernel access tested against its buffer's extent).
+LIB_PATH = os.path.join(_HERE, "libzero_checked.so" if os.environ.get("ZERO_CHECKED") == "1"
+                        else "libzero.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "zero.h")
 
 ZERO_OK = 0
@@ -78,6 +81,14 @@ class zero_adam_t(ctypes.Structure):
 ZERO_ADAM_STATE_BYTES = 32
 
 
+class zero_bounds_t(ctypes.Structure):
+    _fields_ = [("checked", c_i32), ("site", c_i32), ("count", c_i64), ("index", c_i64),
+                ("lo", c_i64), ("hi", c_i64)]
+
+
+ZERO_SITE_PROBE = 1
+
+
 def adam_hp(step: int, grad_scale: float, lr: float = 1e-3, beta1: float = 0.9,
             beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
             d_state=None) -> zero_adam_t:
@@ -122,6 +133,8 @@ _SIGS = {
     "zero_reduce_scatter_norm_static": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_i64, c_i64,
                                                 ctypes.c_float, ctypes.c_float, c_vp, c_vp,
                                                 c_vp]),
+    "zero_bounds_report": (c_i32, [P(zero_bounds_t), c_i32]),
+    "zero_bounds_probe": (c_i32, [c_vp]),
 }
 
 _LIB = None
@@ -379,3 +392,15 @@ def zero_reduce_scatter_norm_static(plan, group, grads, gdtype, reduced, begin, 
     _check(_lib().zero_reduce_scatter_norm_static(
         plan, group, _ptr_array(grads), gdtype, _ptr(reduced), begin, end, grad_scale, max_norm,
         _ptr(d_norm), _ptr(d_coef), _stream(stream)), "zero_reduce_scatter_norm_static")
+
+
+def zero_bounds_report(reset: bool = False) -> dict:
+    """The checked build's record of out-of-extent kernel accesses on the
+    current device (synchronizes it); the release build reports checked = 0."""
+    b = zero_bounds_t()
+    _check(_lib().zero_bounds_report(ctypes.byref(b), 1 if reset else 0), "zero_bounds_report")
+    return {k: getattr(b, k) for k, _ in zero_bounds_t._fields_}
+
+
+def zero_bounds_probe(stream=None) -> None:
+    _check(_lib().zero_bounds_probe(_stream(stream)), "zero_bounds_probe")

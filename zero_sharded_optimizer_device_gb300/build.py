@@ -17,6 +17,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libzero.so")
+# Same sources with -DZERO_CHECKED: every kernel access tested against its
+# buffer's extent and recorded when outside (zero_bounds_report in zero.h).
+LIB_CHECKED = os.path.join(HERE, "libzero_checked.so")
 
 SOURCES = ["zero_plan.cpp", "zero_api.cpp", "zero_sched.cpp", "zero_rs.cu", "zero_kernels.cu",
            "zero_noalloc.cu"]
@@ -33,8 +36,8 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra: list[str], outdir: str = BUILD) -> str:
+    obj = os.path.join(outdir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *COMMON, *ARCH, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     if src.endswith(".cpp"):
         cmd[cmd.index("-c"):cmd.index("-c")] = ["-x", "cu"]
@@ -46,20 +49,25 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_info: bool = False, checked: bool = False) -> str:
+    """Compile and link libzero.so, or with ``checked`` libzero_checked.so."""
+    outdir = os.path.join(BUILD, "checked") if checked else BUILD
+    lib = LIB_CHECKED if checked else LIB
+    os.makedirs(outdir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if checked:
+        extra.append("-DZERO_CHECKED")
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
-    cmd = [nvcc(), "-shared", "-cudart", "shared", *ARCH, "-o", LIB, *objs,
+        objs = list(ex.map(lambda s: _compile(s, extra, outdir), SOURCES))
+    cmd = [nvcc(), "-shared", "-cudart", "shared", *ARCH, "-o", lib, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     if verbose:
-        print(f"built {LIB}")
-    return LIB
+        print(f"built {lib}")
+    return lib
 
 
 if __name__ == "__main__":
-    build(verbose=True, ptxas_info="-v" in sys.argv)
+    build(verbose=True, ptxas_info="-v" in sys.argv, checked="--checked" in sys.argv)

@@ -375,3 +375,32 @@ extern "C" int zero_adam_state_advance(const zero_adam_t* hp, void* d_state,
                                            (double)hp->beta1, (double)hp->beta2,
                                            (cudaStream_t)stream));
 }
+
+extern "C" int zero_bounds_report(zero_bounds_t* out, int32_t reset) {
+  if (!out) return ZERO_EINVAL;
+  *out = zero_bounds_t{};
+#ifdef ZERO_CHECKED
+  out->checked = 1;
+  zk::BoundsRec rec[2] = {};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = zk::bounds_rs(&rec[0], reset != 0);
+  if (e == cudaSuccess) e = zk::bounds_kernels(&rec[1], reset != 0);
+  if (e != cudaSuccess) return cuda_status(e);
+  for (const zk::BoundsRec& r : rec) {
+    if (r.count && !out->count) {  // the first unit with a record gives the details
+      out->site = (int32_t)r.site;
+      out->index = r.index;
+      out->lo = r.lo;
+      out->hi = r.hi;
+    }
+    out->count += (int64_t)r.count;
+  }
+#else
+  (void)reset;
+#endif
+  return ZERO_OK;
+}
+
+extern "C" int zero_bounds_probe(zero_stream_t stream) {
+  return cuda_status(zk::launch_bounds_probe((cudaStream_t)stream));
+}

@@ -260,6 +260,52 @@ __device__ __forceinline__ float scaled(float red, const AdamK& h, float coef) {
   return __fmul_rn(__fmul_rn(red, h.scale), coef);
 }
 
+// ------------------------------------------------------------------------
+// Checked build (-DZERO_CHECKED): every global access is first tested
+// against the extent the C ABI gives its buffer, and one outside is skipped
+// and recorded in this translation unit's g_bounds (the first in detail), so
+// an indexing mistake shows as a count the host reads rather than as a memory
+// fault.  The release build compiles every test to `true`.
+// ------------------------------------------------------------------------
+#ifdef ZERO_CHECKED
+static __device__ BoundsRec g_bounds;
+#endif
+
+// True when the access [a, b) lies inside the extent [lo, hi).
+__device__ __forceinline__ bool in_extent(int64_t a, int64_t b, int64_t lo, int64_t hi,
+                                          int site) {
+#ifdef ZERO_CHECKED
+  if (a <= b && a >= lo && b <= hi) return true;
+  if (atomicAdd(&g_bounds.count, 1ull) == 0ull) {
+    g_bounds.site = site;
+    g_bounds.index = a;
+    g_bounds.lo = lo;
+    g_bounds.hi = hi;
+  }
+  return false;
+#else
+  (void)a, (void)b, (void)lo, (void)hi, (void)site;
+  return true;
+#endif
+}
+
+// Host side of the record, one copy per translation unit that includes this
+// header (zeros, and no CUDA call, in the release build).
+static inline cudaError_t bounds_record(BoundsRec* out, bool reset) {
+#ifdef ZERO_CHECKED
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_bounds, sizeof(BoundsRec));
+  if (e == cudaSuccess && reset) {
+    const BoundsRec zero{};
+    e = cudaMemcpyToSymbol(g_bounds, &zero, sizeof(BoundsRec));
+  }
+  return e;
+#else
+  *out = BoundsRec{};
+  (void)reset;
+  return cudaSuccess;
+#endif
+}
+
 // Grid-stride loop helper.
 __device__ __forceinline__ int64_t gtid() {
   return (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

@@ -112,4 +112,16 @@ int occupancy_of(const void* kernel, int threads);
 // Records a CUDA error for zero_last_cuda_error() on this host thread.
 void record_cuda_error(int err);
 
+// Checked build: the out-of-extent record of one translation unit's kernels
+// (device memory of that unit; see in_extent in zero_device.cuh).
+struct BoundsRec {
+  unsigned long long count;
+  long long site, index, lo, hi;
+};
+// Copy the record of zero_rs.cu / zero_kernels.cu to *out, then clear it if
+// `reset`; the release build writes zeros and makes no CUDA call.
+cudaError_t bounds_rs(BoundsRec* out, bool reset);
+cudaError_t bounds_kernels(BoundsRec* out, bool reset);
+cudaError_t launch_bounds_probe(cudaStream_t st);
+
 }  // namespace zk

@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t i = q << 3;
     const int64_t f = g.flat_off + i;
     if (flat_vec_ok && i >= begin && i + 8 <= end) {
+      if (!in_extent(f, f + 8, g.flat_off + begin, g.flat_off + end, ZERO_SITE_ADAM_FLAT))
+        continue;
       const uint4 r0 = ld_once(reduced + f), r1 = ld_once(reduced + f + 4);
       const float4 p0 = ld_state(master + f), p1 = ld_state(master + f + 4);
       const float4 m0 = ld_state(mom + f), m1 = ld_state(mom + f + 4);
@@ -74,6 +76,9 @@ __global__ void __launch_bounds__(kThreads)
       for (int e = 0; e < 8; ++e) {
         const int64_t j = i + e;
         if (j < begin || j >= end) continue;
+        if (!in_extent(f + e, f + e + 1, g.flat_off + begin, g.flat_off + end,
+                       ZERO_SITE_ADAM_FLAT))
+          continue;
         float p = master[f + e], m = mom[f + e], v = var[f + e];
         adam1(p, m, v, scaled(reduced[f + e], h, coef), h);
         master[f + e] = p;
@@ -106,6 +111,7 @@ __global__ void __launch_bounds__(kThreads)
   for (int64_t q = q0 + gtid(); q < q1; q += gstride()) {
     const int64_t i = q << 3;
     if (i >= a && i + 8 <= b) {
+      if (!in_extent(i, i + 8, a, b, ZERO_SITE_CAST_FLAT)) continue;
       const uint4 x0 = ld_once(src + i), x1 = ld_once(src + i + 4);
       if (out_dtype == ZERO_BF16) {
         st_stream(static_cast<uint16_t*>(dst) + i,
@@ -122,6 +128,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int e = 0; e < 8; ++e) {
         const int64_t j = i + e;
         if (j < a || j >= b) continue;
+        if (!in_extent(j, j + 1, a, b, ZERO_SITE_CAST_FLAT)) continue;
         if (out_dtype == ZERO_BF16) static_cast<uint16_t*>(dst)[j] = to_bf16(src[j]);
         else static_cast<float*>(dst)[j] = src[j];
       }
@@ -147,7 +154,8 @@ __global__ void __launch_bounds__(kNormThreads)
     norm_kernel(const double* __restrict__ partials, int64_t n, float max_norm,
                 float* __restrict__ d_norm, float* __restrict__ d_coef) {
   double s = 0.0;
-  for (int64_t i = threadIdx.x; i < n; i += kNormThreads) s += partials[i];
+  for (int64_t i = threadIdx.x; i < n; i += kNormThreads)
+    if (in_extent(i, i + 1, 0, n, ZERO_SITE_NORM)) s += partials[i];
   __shared__ double red[kNormThreads / 32];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
@@ -191,14 +199,21 @@ __global__ void __launch_bounds__(kThreads)
         ++k;
         next += g.S;
       }
-      const char* s = static_cast<const char*>(shards.p[k]) +
-                      (g.rank_off + (j - (int64_t)k * g.S)) * ES;
+      const int64_t so = g.rank_off + (j - (int64_t)k * g.S);
+      if (!in_extent(k, k + 1, 0, g.n, ZERO_SITE_GATHER_SHARD) ||
+          !in_extent(so, so + VW, g.rank_off, g.rank_off + g.S, ZERO_SITE_GATHER_SHARD) ||
+          !in_extent(j, j + VW, 0, psi_pad, ZERO_SITE_GATHER_OUT))
+        continue;
+      const char* s = static_cast<const char*>(shards.p[k]) + so * ES;
       st_stream(static_cast<char*>(out) + j * ES, ld_once(s));
     }
   } else {
     for (int64_t j = gtid(); j < psi_pad; j += gstride()) {
       const int k = owner_of(j, g);
       const int64_t src = g.rank_off + (j - (int64_t)k * g.S);
+      if (!in_extent(src, src + 1, g.rank_off, g.rank_off + g.S, ZERO_SITE_GATHER_SHARD) ||
+          !in_extent(j, j + 1, 0, psi_pad, ZERO_SITE_GATHER_OUT))
+        continue;
       if (ES == 2)
         static_cast<uint16_t*>(out)[j] = static_cast<const uint16_t*>(shards.p[k])[src];
       else
@@ -229,6 +244,7 @@ __global__ void __launch_bounds__(kThreads)
   unsigned long long s = 0;
   const int64_t nv = n >> 3;
   for (int64_t q = gtid(); q < nv; q += gstride()) {
+    if (!in_extent(q * 8, q * 8 + 8, 0, n, ZERO_SITE_CHECKSUM)) continue;
     const uint4 x = ld_once(bits + q * 8);
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     const int64_t j0 = q * 8;
@@ -240,7 +256,8 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
   for (int64_t j = (nv << 3) + gtid(); j < n; j += gstride())
-    s += (unsigned long long)bits[j] * (1ull + (unsigned long long)(j & 0xFFFF));
+    if (in_extent(j, j + 1, 0, n, ZERO_SITE_CHECKSUM))
+      s += (unsigned long long)bits[j] * (1ull + (unsigned long long)(j & 0xFFFF));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
   if ((threadIdx.x & 31) == 0 && s != 0) atomicAdd(out, s);
@@ -260,7 +277,8 @@ cudaError_t launch_checksum(const void* layer, int64_t n, uint64_t* out, cudaStr
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
     copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t nv) {
-  for (int64_t q = gtid(); q < nv; q += gstride()) st_stream(dst + q, ld_once(src + q));
+  for (int64_t q = gtid(); q < nv; q += gstride())
+    if (in_extent(q, q + 1, 0, nv, ZERO_SITE_COPY)) st_stream(dst + q, ld_once(src + q));
 }
 
 cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t st) {
@@ -325,6 +343,26 @@ cudaError_t launch_adam_state(AdamState* st, const AdamState* init, double b1, d
   AdamState z{};
   adam_state_kernel<<<1, 1, 0, s>>>(st, init ? *init : z, init ? 1 : 0, b1, b2);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Checked build: this unit's out-of-extent record, and a probe kernel that
+// records one (index 1 outside [0, 1)) without making any memory access.
+// ---------------------------------------------------------------------------
+cudaError_t bounds_kernels(BoundsRec* out, bool reset) { return bounds_record(out, reset); }
+
+#ifdef ZERO_CHECKED
+__global__ void bounds_probe_kernel() { (void)in_extent(1, 2, 0, 1, ZERO_SITE_PROBE); }
+#endif
+
+cudaError_t launch_bounds_probe(cudaStream_t st) {
+#ifdef ZERO_CHECKED
+  bounds_probe_kernel<<<1, 1, 0, st>>>();
+  return cudaGetLastError();
+#else
+  (void)st;
+  return cudaSuccess;
+#endif
 }
 
 }  // namespace zk

@@ -113,6 +113,10 @@ __global__ void __launch_bounds__(kThreads)
     const int k = owner_of(i, g);
     float* out = reduced + g.flat_off + i;  // not dereferenced in RS_NORM_ONLY
     if (flat_vec_ok && i >= begin && i + 8 <= end && i + 7 < (int64_t)(k + 1) * g.S) {
+      if (!in_extent(i, i + 8, (int64_t)k * g.S, (int64_t)(k + 1) * g.S, ZERO_SITE_RS_OWNER) ||
+          !in_extent(i, i + 8, 0, (int64_t)n * g.S, ZERO_SITE_RS_GRAD) ||
+          !in_extent(i, i + 8, begin, end, ZERO_SITE_RS_FLAT))
+        continue;
       float acc[8];
       ring_sum8<NT, GT>(src, n, k, i, acc);
       if (mode == RS_ACCUMULATE) {  // previous micro-batches first, then this one
@@ -139,7 +143,13 @@ __global__ void __launch_bounds__(kThreads)
       for (int e = 0; e < 8; ++e) {
         const int64_t j = i + e;
         if (j < begin || j >= end) continue;
-        float r = ring_sum1<GT>(src, n, owner_of(j, g), j);
+        const int kj = owner_of(j, g);
+        if (!in_extent(j, j + 1, (int64_t)kj * g.S, (int64_t)(kj + 1) * g.S,
+                       ZERO_SITE_RS_OWNER) ||
+            !in_extent(j, j + 1, 0, (int64_t)n * g.S, ZERO_SITE_RS_GRAD) ||
+            !in_extent(j, j + 1, begin, end, ZERO_SITE_RS_FLAT))
+          continue;
+        float r = ring_sum1<GT>(src, n, kj, j);
         if (mode == RS_ACCUMULATE) r = __fadd_rn(out[e], r);
         if (mode != RS_NORM_ONLY) out[e] = r;
         const float x = __fmul_rn(r, scale);
@@ -186,6 +196,11 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t f = g.flat_off + i;
     const int k = owner_of(i, g);
     if (flat_vec_ok && i >= begin && i + 8 <= end && i + 7 < (int64_t)(k + 1) * g.S) {
+      if (!in_extent(i, i + 8, (int64_t)k * g.S, (int64_t)(k + 1) * g.S,
+                     ZERO_SITE_STEP_OWNER) ||
+          !in_extent(i, i + 8, 0, (int64_t)n * g.S, ZERO_SITE_STEP_GRAD) ||
+          !in_extent(f, f + 8, g.flat_off + begin, g.flat_off + end, ZERO_SITE_STEP_FLAT))
+        continue;
       const float4 p0 = ld_state(master + f), p1 = ld_state(master + f + 4);
       const float4 m0 = ld_state(mom + f), m1 = ld_state(mom + f + 4);
       const float4 v0 = ld_state(var + f), v1 = ld_state(var + f + 4);
@@ -211,7 +226,9 @@ __global__ void __launch_bounds__(kThreads)
         st_stream(o, make_float4(p[0], p[1], p[2], p[3]));
         st_stream(o + 4, make_float4(p[4], p[5], p[6], p[7]));
       } else if (out_mode == OUT_SHARDS_BF16) {
-        uint16_t* o = static_cast<uint16_t*>(shards.p[k]) + g.rank_off + (i - (int64_t)k * g.S);
+        const int64_t so = g.rank_off + (i - (int64_t)k * g.S);
+        if (!in_extent(so, so + 8, g.rank_off, g.rank_off + g.S, ZERO_SITE_STEP_SHARD)) continue;
+        uint16_t* o = static_cast<uint16_t*>(shards.p[k]) + so;
         if (shard_vec_ok) {
           st_stream(o, make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
                                   pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7])));
@@ -225,6 +242,15 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t j = i + e;
         if (j < begin || j >= end) continue;
         const int kj = owner_of(j, g);
+        const int64_t so = g.rank_off + (j - (int64_t)kj * g.S);
+        if (!in_extent(j, j + 1, (int64_t)kj * g.S, (int64_t)(kj + 1) * g.S,
+                       ZERO_SITE_STEP_OWNER) ||
+            !in_extent(j, j + 1, 0, (int64_t)n * g.S, ZERO_SITE_STEP_GRAD) ||
+            !in_extent(f + e, f + e + 1, g.flat_off + begin, g.flat_off + end,
+                       ZERO_SITE_STEP_FLAT) ||
+            (out_mode == OUT_SHARDS_BF16 &&
+             !in_extent(so, so + 1, g.rank_off, g.rank_off + g.S, ZERO_SITE_STEP_SHARD)))
+          continue;
         const float r = ring_sum1<GT>(src, n, kj, j);
         float p = master[f + e], m = mom[f + e], v = var[f + e];
         adam1(p, m, v, scaled(r, h, coef), h);
@@ -236,7 +262,7 @@ __global__ void __launch_bounds__(kThreads)
         } else if (out_mode == OUT_FULL_F32) {
           static_cast<float*>(out_full)[f + e] = p;
         } else if (out_mode == OUT_SHARDS_BF16) {
-          static_cast<uint16_t*>(shards.p[kj])[g.rank_off + (j - (int64_t)kj * g.S)] = to_bf16(p);
+          static_cast<uint16_t*>(shards.p[kj])[so] = to_bf16(p);
         }
       }
     }
@@ -357,6 +383,8 @@ cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64
   return dispatch<FusedLaunch>(g.n, gdtype, src, g, begin, end, master, m, v, h, coef,
                                out_mode, out_full, shards, st);
 }
+
+cudaError_t bounds_rs(BoundsRec* out, bool reset) { return bounds_record(out, reset); }
 
 }  // namespace zk
 
