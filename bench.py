@@ -467,6 +467,17 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist) -> dict:
 
 
 # ------------------------------------------- stage 3: step + per-layer gathers --
+# Rounds of the arithmetic-bound stand-in consumer (zero_layer_checksum): at 64
+# its 68 launches over the Llama-7B groups take about 3.5x the gathers.
+ARITH_ROUNDS = 64
+
+
+def _hidden(gathers_ms: float, consumers_ms: float, schedule_ms: float) -> float:
+    """Fraction of the shorter of the two kernel streams that the two-stream
+    schedule hides behind the other: 1 = fully overlapped, 0 = serial."""
+    return (gathers_ms + consumers_ms - schedule_ms) / min(gathers_ms, consumers_ms)
+
+
 def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False) -> dict:
     """Stage 3 (the Llama-7B workload): per layer group, in reverse order, a
     fused reduce-scatter + Adam writing each owner's bf16 shard (gradients
@@ -516,15 +527,21 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
 
     order = list(range(len(groups))) + list(reversed(range(len(groups))))
 
-    def gather_schedule():
+    def gather_schedule(rounds):
         """Prefetch on stream B into the free buffer, consume on stream A
         (the library's native two-stream schedule)."""
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(sa)
-        Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, sa, sb)
+        Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, rounds, sa, sb)
         e1.record(sa)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
+
+    def consumers_only(rounds):
+        calls = [lambda j=j, gi=gi: Z.zero_layer_checksum(bufs[j % 2], groups[gi]["psi_pad"],
+                                                          rounds, sums[j:j + 1], sa)
+                 for j, gi in enumerate(order)]
+        return sum(_timed_launches(sa, calls))
 
     def gathers_only():
         calls = [lambda j=j, gi=gi: Z.zero_gather_layer(plan, gi, shards, Z.ZERO_BF16,
@@ -548,7 +565,8 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
 
     for s in range(1, warmup + 1):
         rs_adam_step(s)
-        gather_schedule()
+        gather_schedule(1)
+        gather_schedule(ARITH_ROUNDS)
     graph = None
     if use_graph:
         graph = torch.cuda.CUDAGraph()
@@ -556,7 +574,7 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
         gs.wait_stream(sa)
         with torch.cuda.stream(gs):
             with torch.cuda.graph(graph, stream=gs):
-                Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, gs, gsb)
+                Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, 1, gs, gsb)
         sa.wait_stream(gs)
         torch.cuda.synchronize()
 
@@ -571,20 +589,26 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
     if graph is not None:
         gather_schedule_graph()
     rs_ms, sched_ms, gonly_ms, bcast_ms, graph_ms = [], [], [], [], []
+    cons_ms, sched_a_ms, cons_a_ms = [], [], []
     with ClockSampler(dev.index) as clocks:
         dist.barrier()
         for s in range(warmup + 1, warmup + steps + 1):
             rs_ms.append(rs_adam_step(s))
-            sched_ms.append(gather_schedule())
+            sched_ms.append(gather_schedule(1))
+            sched_a_ms.append(gather_schedule(ARITH_ROUNDS))
             if graph is not None:
                 graph_ms.append(gather_schedule_graph())
             gonly_ms.append(gathers_only())
+            cons_ms.append(consumers_only(1))
+            cons_a_ms.append(consumers_only(ARITH_ROUNDS))
             bcast_ms.append(broadcasts_only())
         dist.barrier()
     gather_elems = 2 * sum(g["psi_pad"] for g in groups)
     return dict(rs_ms=statistics.fmean(rs_ms), sched_ms=statistics.fmean(sched_ms),
                 gonly_ms=statistics.fmean(gonly_ms), bcast_ms=statistics.fmean(bcast_ms),
                 graph_ms=statistics.fmean(graph_ms) if graph_ms else None,
+                cons_ms=statistics.fmean(cons_ms), sched_a_ms=statistics.fmean(sched_a_ms),
+                cons_a_ms=statistics.fmean(cons_a_ms),
                 P=P, N=N, groups=len(groups),
                 gather_elems=gather_elems, clocks=clocks.summary())
 
@@ -755,6 +779,12 @@ def secondary_line(w, args, dist) -> dict:
                        "broadcast_gbs": 4 * r["gather_elems"] / (r["bcast_ms"] * 1e-3) / 1e9,
                        "schedule_gbs_incl_consumer": 6 * r["gather_elems"] /
                        (r["sched_ms"] * 1e-3) / 1e9,
+                       "consumers_only_ms": r["cons_ms"],
+                       "hidden": _hidden(r["gonly_ms"], r["cons_ms"], r["sched_ms"]),
+                       "arith_consumer": {
+                           "rounds": ARITH_ROUNDS, "consumers_only_ms": r["cons_a_ms"],
+                           "schedule_ms": r["sched_a_ms"],
+                           "hidden": _hidden(r["gonly_ms"], r["cons_a_ms"], r["sched_a_ms"])},
                        **({"schedule_graph_ms": r["graph_ms"],
                            "schedule_graph_gbs_incl_consumer": 6 * r["gather_elems"] /
                            (r["graph_ms"] * 1e-3) / 1e9} if r["graph_ms"] else {})},

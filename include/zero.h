@@ -278,27 +278,42 @@ int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const*
  * forward and backward; "Communication Optimization": hide the gathering
  * behind computation by prefetching the next layer]: for j = 0..n-1, gather
  * group order[j] (zero_gather_layer) into layer_bufs[j % 2] on stream_b and
- * consume it on stream_a (zero_layer_checksum into d_sums[j], standing in
- * for the layer's computation).  The gather of order[j+1] is queued before
+ * consume it on stream_a (zero_layer_checksum with consumer_rounds into
+ * d_sums[j], standing in for the layer's computation: 1 round is bound by
+ * memory, many rounds by on-chip arithmetic, like a layer's matrix
+ * products).  The gather of order[j+1] is queued before
  * the consumer of order[j], so the two overlap; a buffer is refilled only
  * after the consumer that last read it has finished.  Stream B first waits
  * for the work already queued on stream A; work queued on stream A after the
  * call runs after every gather and consumer.  layer_bufs: 2 device buffers
  * of buf_elems bf16 elements each (>= psi_pad of every group in order);
- * d_sums: n uint64.  stream_a != stream_b.  Uses five CUDA events created
+ * d_sums: n uint64.  1 <= consumer_rounds <= ZERO_MAX_CONSUMER_ROUNDS.
+ * The two kernels overlap only if their blocks fit on an SM together: the
+ * gathers launch at the ZERO_OCC_PREFETCH cap and the consumer at the
+ * ZERO_OCC_CONSUMER cap (4 + 4 of the 8 resident 256-thread blocks by
+ * default; see zero_set_occupancy).
+ * stream_a != stream_b.  Uses five CUDA events created
  * and released inside the call; allocates no device memory.  The call may be
  * captured in a CUDA graph: with stream_a capturing, stream_b joins the
  * capture through those events and rejoins stream_a before the call returns.
  * Errors: EINVAL, EALIGN, ERANGE (group id or buffer size), ECUDA. */
 int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* order, int32_t n,
                             const void* const* shards, void* const* layer_bufs,
-                            int64_t buf_elems, uint64_t* d_sums, zero_stream_t stream_a,
-                            zero_stream_t stream_b);
+                            int64_t buf_elems, uint64_t* d_sums, int32_t consumer_rounds,
+                            zero_stream_t stream_a, zero_stream_t stream_b);
 
 /* zero_layer_checksum: stands in for the layer computation that consumes a
- * gathered buffer: *d_out = sum over j < n of bits[j] * (1 + j mod 65536)
- * mod 2^64, over n bf16 bit patterns. */
-int zero_layer_checksum(const void* layer, int64_t n, uint64_t* d_out, zero_stream_t stream);
+ * gathered buffer of n bf16 bit patterns (no counterpart on the pages).  For
+ * each 8-element vector v (and each element of a ragged tail on its own),
+ * c_v = sum over its j of bits[j] * (1 + j mod 65536); its term is
+ * t_v = c_v * (1 + K + K^2 + ... + K^(rounds-1)) mod 2^64, computed as
+ * rounds - 1 dependent multiply-adds t = t*K + c_v with K =
+ * 6364136223846793005; *d_out = sum of the terms mod 2^64.  rounds = 1 is
+ * the plain checksum, bound by the one read of the layer; larger rounds add
+ * on-chip work only.  1 <= rounds <= ZERO_MAX_CONSUMER_ROUNDS. */
+#define ZERO_MAX_CONSUMER_ROUNDS 4096
+int zero_layer_checksum(const void* layer, int64_t n, int32_t rounds, uint64_t* d_out,
+                        zero_stream_t stream);
 
 /* zero_reduce_scatter_norm_static: the pages have no counterpart to this
  * entry point; it exists for callers that cannot allocate device memory
@@ -354,9 +369,11 @@ int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
 #define ZERO_OCC_FUSED 0  /* zero_step, zero_step_group */
 #define ZERO_OCC_RS 1     /* zero_reduce_scatter, zero_reduce_scatter_acc */
 #define ZERO_OCC_ADAM 2   /* zero_adam_shard */
-#define ZERO_OCC_GATHER 3 /* zero_gather_layer, zero_layer_checksum */
+#define ZERO_OCC_GATHER 3 /* zero_gather_layer */
 #define ZERO_OCC_STREAM 4 /* zero_all_gather, zero_copy */
-#define ZERO_OCC_KINDS 5
+#define ZERO_OCC_CONSUMER 5 /* zero_layer_checksum (also inside the gather pass) */
+#define ZERO_OCC_PREFETCH 6 /* the gathers inside zero_stage3_gather_pass */
+#define ZERO_OCC_KINDS 7
 int zero_set_occupancy(int32_t kind, int32_t blocks_per_sm, int32_t* previous);
 
 /* zero_copy: device-to-device copy of `bytes` (a multiple of 16) with

@@ -433,10 +433,23 @@ def gather_layer(rank_shards):
     return fulls[0], sent, recv
 
 
-def layer_checksum(bits: np.ndarray) -> int:
-    """Checksum a consumer computes over a gathered bf16 layer buffer:
-    sum over j of bits[j] * (1 + (j mod 65536)), mod 2**64."""
+CONSUME_K = 6364136223846793005  # Knuth's MMIX LCG multiplier
+
+
+def layer_checksum(bits: np.ndarray, rounds: int = 1) -> int:
+    """What the stand-in consumer computes over a gathered bf16 layer buffer
+    (no page defines it; it stands in for the layer's computation): the
+    weighted sum c_v of bits[j] * (1 + (j mod 65536)) over each 8-element
+    vector v (each element of a ragged tail on its own), times the geometric
+    sum 1 + K + ... + K^(rounds-1), summed over v, all mod 2**64.  With
+    rounds = 1 it is the plain weighted checksum."""
+    M = 1 << 64
+    geo = sum(pow(CONSUME_K, i, M) for i in range(rounds)) % M
     j = np.arange(bits.size, dtype=np.uint64)
     w = np.uint64(1) + (j & np.uint64(0xFFFF))
     with np.errstate(over="ignore"):
-        return int(np.sum(bits.astype(np.uint64) * w, dtype=np.uint64))
+        terms = bits.astype(np.uint64) * w
+        nv = bits.size // 8
+        c = [int(x) for x in terms[:nv * 8].reshape(nv, 8).sum(axis=1, dtype=np.uint64)]
+    c += [int(x) for x in terms[nv * 8:]]
+    return sum(x * geo for x in c) % M

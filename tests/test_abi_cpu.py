@@ -147,7 +147,10 @@ def test_device_call_argument_errors_return_before_any_launch():
     assert status(Z.zero_all_gather, p, 3, A, A) == Z.ZERO_ERANGE
     assert status(Z.zero_gather_layer, p, 0, good, Z.ZERO_BF16, A + 1) == Z.ZERO_EALIGN
     assert status(Z.zero_grad_norm, A, 4, 0.0, None, None) == Z.ZERO_EINVAL
-    assert status(Z.zero_layer_checksum, A, 10, A + 4) == Z.ZERO_EALIGN
+    assert status(Z.zero_layer_checksum, A, 10, 1, A + 4) == Z.ZERO_EALIGN
+    assert status(Z.zero_layer_checksum, A, 10, 0, A) == Z.ZERO_EINVAL
+    assert status(Z.zero_layer_checksum, A, 10, Z.ZERO_MAX_CONSUMER_ROUNDS + 1, A) == \
+        Z.ZERO_EINVAL
     assert status(Z.zero_copy, A, A, 15) == Z.ZERO_EINVAL
     assert status(Z.zero_wait_flag, A, 1, Z.ZERO_MAX_POLLS + 1, A) == Z.ZERO_EINVAL
     assert status(Z.zero_wait_flag, A + 2, 1, 10, A) == Z.ZERO_EALIGN
@@ -213,7 +216,8 @@ def test_set_occupancy_round_trip_and_limits():
     assert prev >= 1
     assert Z.zero_set_occupancy(Z.ZERO_OCC_ADAM, 0) == 5
     assert Z.zero_set_occupancy(Z.ZERO_OCC_ADAM, 0) == prev     # default restored
-    for kind, n in [(-1, 1), (Z.ZERO_OCC_STREAM + 1, 1), (Z.ZERO_OCC_RS, 33), (0, -1)]:
+    assert Z.zero_set_occupancy(Z.ZERO_OCC_PREFETCH, 0) >= 1    # the last kind exists
+    for kind, n in [(-1, 1), (Z.ZERO_OCC_PREFETCH + 1, 1), (Z.ZERO_OCC_RS, 33), (0, -1)]:
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_set_occupancy(kind, n)
         assert e.value.status == Z.ZERO_EINVAL

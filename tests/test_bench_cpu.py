@@ -52,3 +52,10 @@ def test_algorithmic_bytes_formula():
     assert bench.algorithmic_bytes(8, 124_439_808, 2) == 124_439_808 * 42
     assert bench.algorithmic_bytes(64, 10, 2) == 10 * 154
     assert bench.algorithmic_bytes(8, 10, 4) == 10 * 58
+
+
+def test_overlap_fraction():
+    import bench
+    assert bench._hidden(10.0, 30.0, 30.0) == 1.0     # gathers entirely behind the consumer
+    assert bench._hidden(10.0, 30.0, 40.0) == 0.0     # one after the other
+    assert bench._hidden(8.0, 4.0, 10.0) == 0.5

@@ -152,7 +152,7 @@ def test_llama_7b_stage3_full_size(cuda):
     bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=cuda) for _ in range(2)]
     order = list(range(G)) + list(reversed(range(G)))
     sums = torch.zeros(len(order), dtype=torch.int64, device=cuda)
-    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums,
+    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums, 1,
                               torch.cuda.current_stream(), sb)
     torch.cuda.synchronize()
     # property at any size: each gathered layer is the concatenation of the

@@ -202,7 +202,7 @@ def test_native_gather_schedule_matches_direct_gathers(cuda):
     order = list(range(G)) + list(reversed(range(G)))
     sums = torch.zeros(len(order), dtype=torch.int64, device=cuda)
     sb = torch.cuda.Stream()
-    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums,
+    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums, 1,
                               torch.cuda.current_stream(), sb)
     torch.cuda.synchronize()
     for j, gi in enumerate(order):
@@ -214,12 +214,15 @@ def test_native_gather_schedule_matches_direct_gathers(cuda):
         assert int(sums[j].item()) % (1 << 64) == O.layer_checksum(bits), (j, gi)
     E = Z.ZeroError
     for bad, status in [(dict(order=[G]), Z.ZERO_ERANGE), (dict(buf_elems=10), Z.ZERO_ERANGE),
-                        (dict(stream_b=torch.cuda.current_stream()), Z.ZERO_EINVAL)]:
-        kw = dict(order=order, buf_elems=gmax, stream_b=sb)
+                        (dict(stream_b=torch.cuda.current_stream()), Z.ZERO_EINVAL),
+                        (dict(rounds=0), Z.ZERO_EINVAL),
+                        (dict(rounds=Z.ZERO_MAX_CONSUMER_ROUNDS + 1), Z.ZERO_EINVAL)]:
+        kw = dict(order=order, buf_elems=gmax, stream_b=sb, rounds=1)
         kw.update(bad)
         with pytest.raises(E) as e:
             Z.zero_stage3_gather_pass(c.plan, kw["order"], shards, bufs, kw["buf_elems"], sums,
-                                      torch.cuda.current_stream(), kw["stream_b"])
+                                      kw["rounds"], torch.cuda.current_stream(),
+                                      kw["stream_b"])
         assert e.value.status == status
 
 
@@ -243,19 +246,21 @@ def test_cuda_graph_of_the_stage3_gather_pass(cuda):
     eager = torch.zeros(len(order), dtype=torch.int64, device=cuda)
     replayed = torch.zeros(len(order), dtype=torch.int64, device=cuda)
     cur = torch.cuda.current_stream()
-    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, eager, cur, torch.cuda.Stream())
+    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, eager, 5, cur,
+                              torch.cuda.Stream())
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     s, sb = torch.cuda.Stream(), torch.cuda.Stream()
     s.wait_stream(cur)
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, replayed, s, sb)
+            Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, replayed, 5, s, sb)
     cur.wait_stream(s)
     torch.cuda.synchronize()
     for r in range(N):
         shards[r].copy_(torch.randn(c.info["shard_total"], device=cuda).to(torch.bfloat16))
-    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, eager, cur, torch.cuda.Stream())
+    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, eager, 5, cur,
+                              torch.cuda.Stream())
     torch.cuda.synchronize()
     g.replay()
     torch.cuda.synchronize()

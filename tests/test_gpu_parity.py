@@ -146,7 +146,7 @@ def test_stage3_mini_step_gather_checksum(cuda):
     for gi, g in enumerate(c.groups):
         layer = torch.empty(g["psi_pad"], dtype=torch.bfloat16, device=cuda)
         Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, layer)
-        Z.zero_layer_checksum(layer, g["psi_pad"], sums[gi:gi + 1])
+        Z.zero_layer_checksum(layer, g["psi_pad"], 1, sums[gi:gi + 1])
         torch.cuda.synchronize()
         # oracle: each owner's shard is the bf16 cast of its updated master
         f0, S = g["flat_off"], g["shard"]

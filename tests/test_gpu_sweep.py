@@ -154,8 +154,10 @@ def test_stage3_rank_count_sweep(cuda, n):
     bufs = [torch.empty(max(1, gmax), dtype=torch.bfloat16, device=cuda) for _ in range(2)]
     order = list(range(G)) + list(reversed(range(G)))
     sums = torch.zeros(len(order), dtype=torch.int64, device=cuda)
-    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums,
+    rounds = int(rng.integers(1, 40))       # consumer from memory-bound to arithmetic-bound
+    Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums, rounds,
                               torch.cuda.current_stream(), torch.cuda.Stream())
     torch.cuda.synchronize()
     for j, gi in enumerate(order):
-        assert int(sums[j].item()) % (1 << 64) == O.layer_checksum(want[gi]), (what, j, gi)
+        assert int(sums[j].item()) % (1 << 64) == O.layer_checksum(want[gi], rounds), \
+            (what, rounds, j, gi)

@@ -331,6 +331,30 @@ def test_layer_checksum_small_case():
     assert O.layer_checksum(big) == 7 * (sum(range(1, 65537)) + 1)
 
 
+def test_consumer_rounds_match_the_iterated_multiply_add():
+    """Brute force on small buffers: per 8-element vector (and per tail
+    element) the consumer's term is rounds - 1 dependent steps t = t*K + c
+    from t = c, mod 2**64; the oracle uses the geometric-sum form."""
+    M = 1 << 64
+    rng = np.random.default_rng(11)
+    for n in (0, 5, 8, 21, 64):
+        bits = rng.integers(0, 1 << 16, n).astype(np.uint16)
+        for rounds in (1, 2, 3, 17):
+            total = 0
+            starts = list(range(0, n - n % 8, 8)) + list(range(n - n % 8, n))
+            for a in starts:
+                b = a + 8 if a < n - n % 8 else a + 1
+                c = sum(int(bits[j]) * (1 + (j % 65536)) for j in range(a, b)) % M
+                t = c
+                for _ in range(rounds - 1):
+                    t = (t * O.CONSUME_K + c) % M
+                total = (total + t) % M
+            assert O.layer_checksum(bits, rounds) == total, (n, rounds)
+    # one element, two rounds: the term is c * (1 + K)
+    one = np.array([3], dtype=np.uint16)
+    assert O.layer_checksum(one, 2) == (3 * (1 + O.CONSUME_K)) % M
+
+
 # ---------------------------------------- whole step: invariants and negatives --
 def test_step_window_equals_full_step():
     w = W.TINY

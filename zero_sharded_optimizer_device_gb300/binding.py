@@ -32,7 +32,9 @@ ZERO_F32 = 0
 ZERO_BF16 = 1
 ZERO_MAX_RANKS = 64
 ZERO_MAX_POLLS = 10_000_000
-ZERO_OCC_FUSED, ZERO_OCC_RS, ZERO_OCC_ADAM, ZERO_OCC_GATHER, ZERO_OCC_STREAM = range(5)
+ZERO_OCC_FUSED, ZERO_OCC_RS, ZERO_OCC_ADAM, ZERO_OCC_GATHER, ZERO_OCC_STREAM, \
+    ZERO_OCC_CONSUMER, ZERO_OCC_PREFETCH = range(7)
+ZERO_MAX_CONSUMER_ROUNDS = 4096
 
 _NAMES = {0: "ZERO_OK", -1: "ZERO_EINVAL", -2: "ZERO_EALIGN", -3: "ZERO_ERANGE",
           -4: "ZERO_EDTYPE", -5: "ZERO_ENOMEM", -6: "ZERO_ECUDA", -7: "ZERO_ETIMEOUT"}
@@ -122,9 +124,9 @@ _SIGS = {
     "zero_step_group": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp,
                                 P(zero_adam_t), c_vp, P(c_vp), c_vp]),
     "zero_gather_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
-    "zero_layer_checksum": (c_i32, [c_vp, c_i64, c_vp, c_vp]),
+    "zero_layer_checksum": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp]),
     "zero_stage3_gather_pass": (c_i32, [c_vp, P(c_i32), c_i32, P(c_vp), P(c_vp), c_i64, c_vp,
-                                        c_vp, c_vp]),
+                                        c_i32, c_vp, c_vp]),
     "zero_copy": (c_i32, [c_vp, c_vp, c_i64, c_vp]),
     "zero_adam_state_init": (c_i32, [P(zero_adam_t), c_vp, c_vp]),
     "zero_adam_state_advance": (c_i32, [P(zero_adam_t), c_vp, c_vp]),
@@ -342,17 +344,17 @@ def zero_gather_layer(plan, group, shards, dtype, layer_out, stream=None) -> Non
                                     _stream(stream)), "zero_gather_layer")
 
 
-def zero_stage3_gather_pass(plan, order, shards, layer_bufs, buf_elems, d_sums, stream_a,
-                            stream_b) -> None:
+def zero_stage3_gather_pass(plan, order, shards, layer_bufs, buf_elems, d_sums,
+                            consumer_rounds, stream_a, stream_b) -> None:
     arr = (c_i32 * max(1, len(order)))(*[int(g) for g in order])
     _check(_lib().zero_stage3_gather_pass(plan, arr, len(order), _ptr_array(shards),
                                           _ptr_array(layer_bufs), buf_elems, _ptr(d_sums),
-                                          _stream(stream_a), _stream(stream_b)),
+                                          consumer_rounds, _stream(stream_a), _stream(stream_b)),
            "zero_stage3_gather_pass")
 
 
-def zero_layer_checksum(layer, n, d_out, stream=None) -> None:
-    _check(_lib().zero_layer_checksum(_ptr(layer), n, _ptr(d_out), _stream(stream)),
+def zero_layer_checksum(layer, n, rounds, d_out, stream=None) -> None:
+    _check(_lib().zero_layer_checksum(_ptr(layer), n, rounds, _ptr(d_out), _stream(stream)),
            "zero_layer_checksum")
 
 

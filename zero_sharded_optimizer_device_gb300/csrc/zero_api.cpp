@@ -318,16 +318,17 @@ extern "C" int zero_gather_layer(const zero_plan_t* plan, int32_t group, const v
   ZERO_TRY(check_buf(layer_out));
   return cuda_status(zk::launch_gather(rank_ptrs(plan, shards), dtype == ZERO_BF16 ? 2 : 4,
                                        group_k(plan, group), plan->groups[group].psi_pad,
-                                       layer_out, (cudaStream_t)stream));
+                                       layer_out, ZERO_OCC_GATHER, (cudaStream_t)stream));
 }
 
-extern "C" int zero_layer_checksum(const void* layer, int64_t n, uint64_t* d_out,
-                                   zero_stream_t stream) {
+extern "C" int zero_layer_checksum(const void* layer, int64_t n, int32_t rounds,
+                                   uint64_t* d_out, zero_stream_t stream) {
   NvtxRange nvtx("zero_layer_checksum");
   if (n < 0 || !d_out || (n > 0 && !layer)) return ZERO_EINVAL;
+  if (rounds < 1 || rounds > ZERO_MAX_CONSUMER_ROUNDS) return ZERO_EINVAL;
   ZERO_TRY(check_opt_buf(layer));
   if (((uintptr_t)d_out & 7u) != 0) return ZERO_EALIGN;
-  return cuda_status(zk::launch_checksum(layer, n, d_out, (cudaStream_t)stream));
+  return cuda_status(zk::launch_checksum(layer, n, rounds, d_out, (cudaStream_t)stream));
 }
 
 extern "C" int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_t stream) {

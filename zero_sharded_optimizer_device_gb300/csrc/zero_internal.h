@@ -92,10 +92,13 @@ cudaError_t launch_cast(const float* src, int64_t a, int64_t b, int out_dtype, v
 cudaError_t launch_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
                         float* d_coef, cudaStream_t st);
 
+// occ_kind: the occupancy cap to launch with (ZERO_OCC_GATHER standalone,
+// ZERO_OCC_PREFETCH inside the two-stream gather pass).
 cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
-                          int64_t psi_pad, void* out, cudaStream_t st);
+                          int64_t psi_pad, void* out, int occ_kind, cudaStream_t st);
 
-cudaError_t launch_checksum(const void* layer, int64_t n, uint64_t* out, cudaStream_t st);
+cudaError_t launch_checksum(const void* layer, int64_t n, int rounds, uint64_t* out,
+                            cudaStream_t st);
 
 cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t st);
 

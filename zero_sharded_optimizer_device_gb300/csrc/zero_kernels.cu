@@ -3,7 +3,7 @@
 //   cast_kernel     all-gather of the updated parameters into the full buffer
 //   norm_kernel     global gradient norm and clip coefficient
 //   gather_kernel   stage-3 per-layer gather of N rank shards
-//   checksum_kernel consumer of a gathered layer
+//   checksum_kernel consumer of a gathered layer (stands in for its computation)
 //   copy_kernel     16-byte device copy (achievable HBM bandwidth)
 #include "zero_device.cuh"
 
@@ -223,23 +223,35 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
-                          int64_t psi_pad, void* out, cudaStream_t st) {
+                          int64_t psi_pad, void* out, int occ_kind, cudaStream_t st) {
   if (psi_pad <= 0) return cudaSuccess;
   if (elem_bytes == 2) {
-    gather_kernel<2><<<(unsigned)wave_grid(gather_kernel<2>, psi_pad / 8 + 1, ZERO_OCC_GATHER), kThreads, 0, st>>>(
-        shards, g, psi_pad, out);
+    gather_kernel<2><<<(unsigned)wave_grid(gather_kernel<2>, psi_pad / 8 + 1, occ_kind), kThreads,
+                       0, st>>>(shards, g, psi_pad, out);
   } else {
-    gather_kernel<4><<<(unsigned)wave_grid(gather_kernel<4>, psi_pad / 4 + 1, ZERO_OCC_GATHER), kThreads, 0, st>>>(
-        shards, g, psi_pad, out);
+    gather_kernel<4><<<(unsigned)wave_grid(gather_kernel<4>, psi_pad / 4 + 1, occ_kind), kThreads,
+                       0, st>>>(shards, g, psi_pad, out);
   }
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// Layer consumer: sum of bits[j] * (1 + (j mod 65536)), mod 2^64.
+// Layer consumer (stands in for the layer's computation): for each 8-element
+// vector, c = sum of bits[j] * (1 + (j mod 65536)); its term is c after
+// rounds - 1 dependent multiply-adds t = t*K + c, i.e. c * (1 + K + ... +
+// K^(rounds-1)) mod 2^64.  The on-chip work grows with rounds while the
+// memory traffic stays one read of the layer.
 // ---------------------------------------------------------------------------
+constexpr unsigned long long kConsumeK = 6364136223846793005ull;  // Knuth's MMIX LCG multiplier
+
+__device__ __forceinline__ unsigned long long consume_term(unsigned long long c, int rounds) {
+  unsigned long long t = c;
+  for (int r = 1; r < rounds; ++r) t = t * kConsumeK + c;
+  return t;
+}
+
 __global__ void __launch_bounds__(kThreads)
-    checksum_kernel(const uint16_t* __restrict__ bits, int64_t n,
+    checksum_kernel(const uint16_t* __restrict__ bits, int64_t n, int rounds,
                     unsigned long long* __restrict__ out) {
   unsigned long long s = 0;
   const int64_t nv = n >> 3;
@@ -248,27 +260,32 @@ __global__ void __launch_bounds__(kThreads)
     const uint4 x = ld_once(bits + q * 8);
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     const int64_t j0 = q * 8;
+    unsigned long long c = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int64_t j = j0 + 2 * e;
-      s += (unsigned long long)(w[e] & 0xFFFFu) * (1ull + (unsigned long long)(j & 0xFFFF));
-      s += (unsigned long long)(w[e] >> 16) * (1ull + (unsigned long long)((j + 1) & 0xFFFF));
+      c += (unsigned long long)(w[e] & 0xFFFFu) * (1ull + (unsigned long long)(j & 0xFFFF));
+      c += (unsigned long long)(w[e] >> 16) * (1ull + (unsigned long long)((j + 1) & 0xFFFF));
     }
+    s += consume_term(c, rounds);
   }
   for (int64_t j = (nv << 3) + gtid(); j < n; j += gstride())
     if (in_extent(j, j + 1, 0, n, ZERO_SITE_CHECKSUM))
-      s += (unsigned long long)bits[j] * (1ull + (unsigned long long)(j & 0xFFFF));
+      s += consume_term((unsigned long long)bits[j] * (1ull + (unsigned long long)(j & 0xFFFF)),
+                        rounds);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
   if ((threadIdx.x & 31) == 0 && s != 0) atomicAdd(out, s);
 }
 
-cudaError_t launch_checksum(const void* layer, int64_t n, uint64_t* out, cudaStream_t st) {
+cudaError_t launch_checksum(const void* layer, int64_t n, int rounds, uint64_t* out,
+                            cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(out, 0, sizeof(uint64_t), st);
   if (e != cudaSuccess) return e;
   if (n <= 0) return cudaSuccess;
-  checksum_kernel<<<(unsigned)wave_grid(checksum_kernel, n / 8 + 1, ZERO_OCC_GATHER), kThreads, 0, st>>>(
-      static_cast<const uint16_t*>(layer), n, reinterpret_cast<unsigned long long*>(out));
+  checksum_kernel<<<(unsigned)wave_grid(checksum_kernel, n / 8 + 1, ZERO_OCC_CONSUMER), kThreads,
+                    0, st>>>(static_cast<const uint16_t*>(layer), n, rounds,
+                             reinterpret_cast<unsigned long long*>(out));
   return cudaGetLastError();
 }
 

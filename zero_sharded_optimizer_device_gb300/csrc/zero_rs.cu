@@ -47,14 +47,20 @@ namespace {
 // fused N=8 step 3 (6699; 6326 at 2, 6097 at 4), fused N=16 3 (7069), Adam
 // 2 (6418; 5775 at 4), reduce-scatter with norm partials 8 (6550-6732;
 // 5780 at 3), stage-3 gather 8 (6522; 4444 at 3), all-gather cast 4 (6494).
+// Two-stream gather pass over the Llama-7B groups (ms for 68 gathers +
+// consumers): prefetch 4 + consumer 4 gave 12.6 with the one-read consumer
+// and 58.3 with a 128-round one, against 14.5 and 61.3 at 8 + 8, where the
+// two kernels cannot share an SM and run one after the other.
 constexpr int kOccDefault[ZERO_OCC_KINDS] = {
     3,   // ZERO_OCC_FUSED
     8,   // ZERO_OCC_RS
     2,   // ZERO_OCC_ADAM
     8,   // ZERO_OCC_GATHER
     4,   // ZERO_OCC_STREAM
+    4,   // ZERO_OCC_CONSUMER
+    4,   // ZERO_OCC_PREFETCH
 };
-std::atomic<int> g_occ[ZERO_OCC_KINDS] = {{0}, {0}, {0}, {0}, {0}};
+std::atomic<int> g_occ[ZERO_OCC_KINDS] = {{0}, {0}, {0}, {0}, {0}, {0}, {0}};
 }  // namespace
 
 int occupancy_cap(int kind) {

@@ -5,7 +5,11 @@
 // forward and again in the backward pass; "Communication Optimization":
 // parameter gathering is hidden behind computation by prefetching the next
 // layer.  Here the gather of the next group runs on stream B into the free
-// one of two layer buffers while stream A consumes the current one.
+// one of two layer buffers while stream A consumes the current one.  The two
+// kernels can only run at the same time if their blocks fit on an SM
+// together, so the gathers launch with their own occupancy cap
+// (ZERO_OCC_PREFETCH, default 4 of the 8 resident 256-thread blocks)
+// beside the consumer's (ZERO_OCC_CONSUMER, default 4).
 #include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
@@ -35,9 +39,11 @@ struct Events {
 extern "C" int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* order, int32_t n,
                                        const void* const* shards, void* const* layer_bufs,
                                        int64_t buf_elems, uint64_t* d_sums,
-                                       zero_stream_t stream_a, zero_stream_t stream_b) {
+                                       int32_t consumer_rounds, zero_stream_t stream_a,
+                                       zero_stream_t stream_b) {
   if (!plan || n < 0 || (n > 0 && (!order || !layer_bufs || !d_sums)) || !shards)
     return ZERO_EINVAL;
+  if (consumer_rounds < 1 || consumer_rounds > ZERO_MAX_CONSUMER_ROUNDS) return ZERO_EINVAL;
   if (n == 0) return ZERO_OK;
   if (stream_a == stream_b) return ZERO_EINVAL;
   for (int r = 0; r < plan->n_ranks; ++r) {
@@ -75,7 +81,7 @@ extern "C" int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* o
     if (j >= 2) r = cudaStreamWaitEvent(sb, ev.e[3 + (j & 1)], 0);
     if (r == cudaSuccess)
       r = zk::launch_gather(src, 2, gk(order[j]), plan->groups[order[j]].psi_pad,
-                            layer_bufs[j & 1], sb);
+                            layer_bufs[j & 1], ZERO_OCC_PREFETCH, sb);
     if (r == cudaSuccess) r = cudaEventRecord(ev.e[1 + (j & 1)], sb);
     return r;
   };
@@ -88,7 +94,8 @@ extern "C" int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* o
     if (j + 1 < n) e = issue(j + 1);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(sa, ev.e[1 + (j & 1)], 0);
     if (e == cudaSuccess)
-      e = zk::launch_checksum(layer_bufs[j & 1], plan->groups[order[j]].psi_pad, d_sums + j, sa);
+      e = zk::launch_checksum(layer_bufs[j & 1], plan->groups[order[j]].psi_pad, consumer_rounds,
+                              d_sums + j, sa);
     if (e == cudaSuccess) e = cudaEventRecord(ev.e[3 + (j & 1)], sa);
   }
   nvtxRangePop();
