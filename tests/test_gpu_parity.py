@@ -275,6 +275,90 @@ def test_outputs_stay_inside_their_buffers(cuda):
         assert bool((b[:G] == -12345.0).all()) and bool((b[-G:] == -12345.0).all()), name
 
 
+def test_windowed_calls_write_only_their_window(cuda):
+    """Reduce-scatter (store and accumulate), Adam and the fused step on a
+    window [a, b) leave every element of their flat outputs outside it as it
+    was; norm partials are written only in [0, zero_rs_partials)."""
+    import torch
+    c = Case([5000, 1337, 21], 4, 1, "bf16", seed=23, host_state=False)
+    Z = c.Z
+    P = c.info["psi_pad"]
+    a, b = 1003, P - 997                      # ragged: cuts 8-element vectors on both ends
+    grads = c.grads_dev(0, 1)
+    mark = -12345.0
+
+    def flat(dtype=torch.float32):
+        return torch.full((P,), mark, dtype=dtype, device=cuda)
+
+    def untouched(t, what):
+        fill = torch.tensor(mark, dtype=t.dtype, device=cuda)   # the mark in t's dtype
+        outside = torch.cat([t[:a], t[b:]])
+        assert bool((outside == fill).all()), what
+        assert not bool((t[a:b] == fill).any()), what + " (window not written)"
+
+    red = flat()
+    k = Z.zero_rs_partials(c.plan, Z.ZERO_BF16, b - a)
+    part = torch.full((k + 64,), mark, dtype=torch.float64, device=cuda)
+    Z.zero_reduce_scatter(c.plan, 0, grads, Z.ZERO_BF16, red, a, b, 0.25, part)
+    torch.cuda.synchronize()
+    untouched(red, "reduce-scatter")
+    assert bool((part[k:] == mark).all()) and not bool((part[:k] == mark).any())
+    Z.zero_reduce_scatter_acc(c.plan, 0, grads, Z.ZERO_BF16, red, a, b, 0.25)
+    torch.cuda.synchronize()
+    untouched(red, "accumulate")
+    master, m, v = flat(), flat(), flat()
+    master[a:b] = 0.5
+    m[a:b] = 0.0
+    v[a:b] = 0.0
+    out = flat(torch.bfloat16)
+    Z.zero_adam_shard(c.plan, 0, master, m, v, red, c.hp_dev(1), None, a, b, out, Z.ZERO_BF16)
+    torch.cuda.synchronize()
+    for t, name in ((master, "adam master"), (m, "adam m"), (v, "adam v"), (out, "adam out")):
+        untouched(t, name)
+    out32 = flat()
+    Z.zero_all_gather(c.plan, 0, master, out32, Z.ZERO_F32)
+    torch.cuda.synchronize()
+    assert torch.equal(out32[a:b], master[a:b])
+
+
+def test_stage3_outputs_stay_inside_their_buffers(cuda):
+    """Guard bands around every rank's shard buffer, the layer buffer, the
+    checksum word and the norm outputs: untouched by the stage-3 step, the
+    gather, the consumer and the norm."""
+    import torch
+    numels = [700, 33, 1200, 5, 810]
+    c = Case(numels, 5, 1, "bf16", seed=29, groups=[0, 0, 1, 1, 2], host_state=False)
+    Z = c.Z
+    G = 64
+
+    def guarded(n, dtype):
+        words = (n * (2 if dtype == torch.bfloat16 else (8 if dtype == torch.int64 else 4)) + 3) // 4
+        buf = torch.full((words + 2 * G,), -12345.0, dtype=torch.float32, device=cuda)
+        return buf, buf[G:G + words].view(dtype)[:n]
+
+    sh = [guarded(c.info["shard_total"], torch.bfloat16) for _ in range(5)]
+    shards = [x[1] for x in sh]
+    for x in shards:
+        x.zero_()
+    for gi in reversed(range(len(c.groups))):
+        Z.zero_step_group(c.plan, gi, c.grads_dev(gi, 1), Z.ZERO_BF16, c.master, c.m, c.v,
+                          c.hp_dev(1), None, shards)
+    gmax = max(g["psi_pad"] for g in c.groups)
+    lb, layer = guarded(gmax, torch.bfloat16)
+    sb, word = guarded(1, torch.int64)
+    nb, norm = guarded(1, torch.float32)
+    cb, coef = guarded(1, torch.float32)
+    part = torch.ones(10, dtype=torch.float64, device=cuda)
+    for gi, g in enumerate(c.groups):
+        Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, layer[:g["psi_pad"]])
+        Z.zero_layer_checksum(layer, g["psi_pad"], 3, word)
+    Z.zero_grad_norm(part, 10, 1.0, norm, coef)
+    torch.cuda.synchronize()
+    for name, (b, _) in [("layer", (lb, None)), ("checksum", (sb, None)), ("norm", (nb, None)),
+                         ("coef", (cb, None))] + [(f"shards {r}", sh[r]) for r in range(5)]:
+        assert bool((b[:G] == -12345.0).all()) and bool((b[-G:] == -12345.0).all()), name
+
+
 # ------------------------------------------------ full size, sampled windows --
 def test_gpt2_small_full_size_sampled(cuda):
     """The workload the benchmark times (fused zero_step, N=8, bf16 grads),
