@@ -269,7 +269,11 @@ int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* g
  * layer's parameters just before use; P2: by all-gather]: layer_out[j] =
  * shards[j / S_g][rank_off(g) + j % S_g] for j in [0, psi_pad(g)): the N
  * ranks' shards of group g concatenated into one contiguous layer buffer.
- * dtype: element type of the shard buffers (ZERO_BF16 or ZERO_F32). */
+ * dtype: element type of the shard buffers (ZERO_BF16 or ZERO_F32).  When
+ * S_g and rank_off(g) are multiples of 16 bytes the N segments move by 1-D
+ * bulk copies (TMA) through shared memory, issued by one thread per CTA;
+ * their waits are bounded (see zero_async_status).  Otherwise 16-byte vector
+ * loads and stores, or single elements where the shards cut vectors. */
 int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
                       zero_dtype_t dtype, void* layer_out, zero_stream_t stream);
 
@@ -290,8 +294,8 @@ int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const*
  * d_sums: n uint64.  1 <= consumer_rounds <= ZERO_MAX_CONSUMER_ROUNDS.
  * The two kernels overlap only if their blocks fit on an SM together: the
  * gathers launch at the ZERO_OCC_PREFETCH cap and the consumer at the
- * ZERO_OCC_CONSUMER cap (4 + 4 of the 8 resident 256-thread blocks by
- * default; see zero_set_occupancy).
+ * ZERO_OCC_CONSUMER cap (by default 2 one-warp bulk-copy CTAs beside 7 of
+ * the 8 resident 256-thread blocks; see zero_set_occupancy).
  * stream_a != stream_b.  Uses five CUDA events created
  * and released inside the call; allocates no device memory.  The call may be
  * captured in a CUDA graph: with stream_a capturing, stream_b joins the
@@ -369,16 +373,24 @@ int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
 #define ZERO_OCC_FUSED 0  /* zero_step, zero_step_group */
 #define ZERO_OCC_RS 1     /* zero_reduce_scatter, zero_reduce_scatter_acc */
 #define ZERO_OCC_ADAM 2   /* zero_adam_shard */
-#define ZERO_OCC_GATHER 3 /* zero_gather_layer */
+#define ZERO_OCC_GATHER 3 /* zero_gather_layer (CTAs per SM of its bulk-copy form) */
 #define ZERO_OCC_STREAM 4 /* zero_all_gather, zero_copy */
 #define ZERO_OCC_CONSUMER 5 /* zero_layer_checksum (also inside the gather pass) */
-#define ZERO_OCC_PREFETCH 6 /* the gathers inside zero_stage3_gather_pass */
+#define ZERO_OCC_PREFETCH 6 /* the gathers inside zero_stage3_gather_pass (as GATHER) */
 #define ZERO_OCC_KINDS 7
 int zero_set_occupancy(int32_t kind, int32_t blocks_per_sm, int32_t* previous);
 
 /* zero_copy: device-to-device copy of `bytes` (a multiple of 16) with
  * 16-byte loads and stores; measures the achievable HBM copy bandwidth. */
 int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_t stream);
+
+/* zero_async_status: number of bounded waits inside the library's kernels
+ * that gave up (a bulk copy that had not landed after about 2 s) on the
+ * current device since the last reset; nonzero means a result is incomplete.
+ * The kernel that gave up still returns (the context stays usable).  No
+ * counterpart on the pages.  Synchronizes the device; reset != 0 clears the
+ * count afterwards.  Errors: EINVAL (timeouts NULL), ECUDA. */
+int zero_async_status(int64_t* timeouts, int32_t reset);
 
 /* ------------------------------------------------------ checked build --
  * No counterpart on the pages: a stand-in for a device memory checker.  The

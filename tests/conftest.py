@@ -37,15 +37,19 @@ def cuda():
 
 @pytest.fixture(autouse=True)
 def _no_out_of_extent_access(request):
-    """Under the bounds-checked library (ZERO_CHECKED=1), every GPU test must
-    leave the kernels' out-of-extent record empty."""
+    """After every GPU test: no bounded device wait gave up, and under the
+    bounds-checked library (ZERO_CHECKED=1) the kernels' out-of-extent
+    record is empty."""
     yield
-    if os.environ.get("ZERO_CHECKED") != "1" or request.node.get_closest_marker("gpu") is None:
+    if request.node.get_closest_marker("gpu") is None:
         return
     import torch
     if not torch.cuda.is_available():
         return
     import zero_sharded_optimizer_device_gb300 as Z
+    assert Z.zero_async_status(reset=True) == 0, "a bounded device wait gave up"
+    if os.environ.get("ZERO_CHECKED") != "1":
+        return
     r = Z.zero_bounds_report(reset=True)
     assert r["checked"] == 1, "ZERO_CHECKED=1 but the release library is loaded"
     assert r["count"] == 0, f"kernel accesses outside their buffer's extent: {r}"

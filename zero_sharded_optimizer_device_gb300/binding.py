@@ -136,6 +136,7 @@ _SIGS = {
                                                 ctypes.c_float, ctypes.c_float, c_vp, c_vp,
                                                 c_vp]),
     "zero_bounds_report": (c_i32, [P(zero_bounds_t), c_i32]),
+    "zero_async_status": (c_i32, [P(c_i64), c_i32]),
     "zero_bounds_probe": (c_i32, [c_vp]),
 }
 
@@ -406,3 +407,10 @@ def zero_bounds_report(reset: bool = False) -> dict:
 
 def zero_bounds_probe(stream=None) -> None:
     _check(_lib().zero_bounds_probe(_stream(stream)), "zero_bounds_probe")
+
+
+def zero_async_status(reset: bool = False) -> int:
+    """Bounded device waits that gave up since the last reset (synchronizes)."""
+    n = c_i64()
+    _check(_lib().zero_async_status(ctypes.byref(n), 1 if reset else 0), "zero_async_status")
+    return n.value

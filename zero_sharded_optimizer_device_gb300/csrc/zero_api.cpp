@@ -405,3 +405,13 @@ extern "C" int zero_bounds_report(zero_bounds_t* out, int32_t reset) {
 extern "C" int zero_bounds_probe(zero_stream_t stream) {
   return cuda_status(zk::launch_bounds_probe((cudaStream_t)stream));
 }
+
+extern "C" int zero_async_status(int64_t* timeouts, int32_t reset) {
+  if (!timeouts) return ZERO_EINVAL;
+  unsigned long long n = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = zk::async_timeouts(&n, reset != 0);
+  if (e != cudaSuccess) return cuda_status(e);
+  *timeouts = (int64_t)n;
+  return ZERO_OK;
+}

@@ -127,4 +127,7 @@ cudaError_t bounds_rs(BoundsRec* out, bool reset);
 cudaError_t bounds_kernels(BoundsRec* out, bool reset);
 cudaError_t launch_bounds_probe(cudaStream_t st);
 
+// Bounded device waits that gave up (zero_async_status), current device.
+cudaError_t async_timeouts(unsigned long long* out, bool reset);
+
 }  // namespace zk

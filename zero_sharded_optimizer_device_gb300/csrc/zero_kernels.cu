@@ -222,17 +222,161 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Stage-3 gather with 1-D bulk copies (TMA).  The layer is N contiguous
+// segments (owner k's S elements land at k*S), cut into pieces of up to
+// kBulkChunk bytes.  One thread per CTA moves its pieces global -> shared ->
+// global through a ring of kBulkStages buffers: a piece's load completes on
+// its stage's mbarrier (expect_tx), its store is a bulk-group copy, and a
+// stage is refilled once the store that read it has finished reading.  Every
+// mbarrier wait gives up after ~2 s: the timeout is counted in
+// g_async_timeouts (zero_async_status), the CTA lets the loads it issued
+// land (again bounded) and returns.  Used when every segment start and length
+// is a multiple of 16 bytes; gather_kernel otherwise.
+// ---------------------------------------------------------------------------
+constexpr int kBulkChunk = 8192;
+constexpr int kBulkStages = 4;
+constexpr int kBulkThreads = 32;       // one warp per CTA; lane 0 issues
+constexpr int kGatherVecBlocks = 8;    // resident blocks per SM of the vector fallback
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+static __device__ unsigned long long g_async_timeouts;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait until the mbarrier's phase of this parity has completed; false after
+// kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+__global__ void __launch_bounds__(kBulkThreads)
+    gather_bulk_kernel(RankPtrs shards, GroupK g, int es, int64_t cps, int64_t nchunks,
+                       char* __restrict__ out) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ __align__(8) uint64_t full[kBulkStages];
+  if (threadIdx.x != 0) return;
+  const uint32_t bar0 = smem_addr(full), buf0 = smem_addr(ring);
+  for (int s = 0; s < kBulkStages; ++s)
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s));
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const int64_t G = gridDim.x, b = blockIdx.x;
+  const int64_t niter = b < nchunks ? (nchunks - b + G - 1) / G : 0;
+  const int64_t segb = g.S * es;
+  // piece i of this CTA: source, destination, bytes (false: outside its
+  // extent, which only the checked build can report)
+  auto piece = [&](int64_t i, const char*& src, char*& dst, uint32_t& bytes) {
+    const int64_t c = b + i * G;
+    const int k = (int)(c / cps);
+    const int64_t off = (c % cps) * kBulkChunk;
+    const int64_t rem = segb - off;
+    bytes = (uint32_t)(rem < kBulkChunk ? rem : kBulkChunk);
+    const int64_t so = g.rank_off + off / es, j = (int64_t)k * g.S + off / es, len = bytes / es;
+    src = static_cast<const char*>(shards.p[k]) + so * es;
+    dst = out + j * es;
+    return in_extent(k, k + 1, 0, g.n, ZERO_SITE_GATHER_SHARD) &&
+           in_extent(so, so + len, g.rank_off, g.rank_off + g.S, ZERO_SITE_GATHER_SHARD) &&
+           in_extent(j, j + len, 0, (int64_t)g.n * g.S, ZERO_SITE_GATHER_OUT);
+  };
+  auto load = [&](int64_t i) {
+    const uint32_t bar = bar0 + 8 * (uint32_t)(i % kBulkStages);
+    const char* src;
+    char* dst;
+    uint32_t bytes;
+    if (piece(i, src, dst, bytes)) {
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                   "r"(bytes)
+                   : "memory");
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+          "[%3];" ::"r"(buf0 + (uint32_t)(i % kBulkStages) * kBulkChunk),
+          "l"(src), "r"(bytes), "r"(bar)
+          : "memory");
+    } else {  // skipped piece: complete the phase with no bytes
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+    }
+  };
+  const int64_t pro = niter < kBulkStages - 1 ? niter : kBulkStages - 1;
+  for (int64_t i = 0; i < pro; ++i) load(i);
+  int64_t loaded = pro, i = 0;
+  for (; i < niter; ++i) {
+    const int s = (int)(i % kBulkStages);
+    if (!mbar_wait(bar0 + 8 * s, (uint32_t)((i / kBulkStages) & 1))) {
+      atomicAdd(&g_async_timeouts, 1ull);
+      break;
+    }
+    const char* src;
+    char* dst;
+    uint32_t bytes;
+    if (piece(i, src, dst, bytes))
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                   "r"(buf0 + (uint32_t)s * kBulkChunk), "r"(bytes)
+                   : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    // refill the stage of piece i - 1 once its store has read it
+    const int64_t next = i + kBulkStages - 1;
+    if (next < niter) {
+      asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      load(next);
+      loaded = next + 1;
+    }
+  }
+  // after a timeout: the loads still in flight land before the CTA exits
+  for (int64_t j = i; j < loaded; ++j)
+    if (!mbar_wait(bar0 + 8 * (int)(j % kBulkStages), (uint32_t)((j / kBulkStages) & 1)))
+      atomicAdd(&g_async_timeouts, 1ull);
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
                           int64_t psi_pad, void* out, int occ_kind, cudaStream_t st) {
   if (psi_pad <= 0) return cudaSuccess;
+  const int64_t segb = g.S * elem_bytes;
+  if (segb % 16 == 0 && (g.rank_off * elem_bytes) % 16 == 0) {
+    const int64_t cps = (segb + kBulkChunk - 1) / kBulkChunk, nchunks = g.n * cps;
+    int64_t grid = (int64_t)sm_count() * occupancy_cap(occ_kind);
+    if (grid > nchunks) grid = nchunks;
+    gather_bulk_kernel<<<(unsigned)grid, kBulkThreads, kBulkStages * kBulkChunk, st>>>(
+        shards, g, elem_bytes, cps, nchunks, static_cast<char*>(out));
+    return cudaGetLastError();
+  }
+  const int64_t wave = (int64_t)sm_count() * kGatherVecBlocks;
   if (elem_bytes == 2) {
-    gather_kernel<2><<<(unsigned)wave_grid(gather_kernel<2>, psi_pad / 8 + 1, occ_kind), kThreads,
-                       0, st>>>(shards, g, psi_pad, out);
+    const int64_t want = psi_pad / 8 / kThreads + 1;
+    gather_kernel<2><<<(unsigned)(want < wave ? want : wave), kThreads, 0, st>>>(shards, g,
+                                                                                psi_pad, out);
   } else {
-    gather_kernel<4><<<(unsigned)wave_grid(gather_kernel<4>, psi_pad / 4 + 1, occ_kind), kThreads,
-                       0, st>>>(shards, g, psi_pad, out);
+    const int64_t want = psi_pad / 4 / kThreads + 1;
+    gather_kernel<4><<<(unsigned)(want < wave ? want : wave), kThreads, 0, st>>>(shards, g,
+                                                                                psi_pad, out);
   }
   return cudaGetLastError();
+}
+
+cudaError_t async_timeouts(unsigned long long* out, bool reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_async_timeouts, sizeof(unsigned long long));
+  if (e == cudaSuccess && reset) {
+    const unsigned long long zero = 0;
+    e = cudaMemcpyToSymbol(g_async_timeouts, &zero, sizeof(zero));
+  }
+  return e;
 }
 
 // ---------------------------------------------------------------------------

@@ -47,18 +47,21 @@ namespace {
 // fused N=8 step 3 (6699; 6326 at 2, 6097 at 4), fused N=16 3 (7069), Adam
 // 2 (6418; 5775 at 4), reduce-scatter with norm partials 8 (6550-6732;
 // 5780 at 3), stage-3 gather 8 (6522; 4444 at 3), all-gather cast 4 (6494).
-// Two-stream gather pass over the Llama-7B groups (ms for 68 gathers +
-// consumers): prefetch 4 + consumer 4 gave 12.6 with the one-read consumer
-// and 58.3 with a 128-round one, against 14.5 and 61.3 at 8 + 8, where the
-// two kernels cannot share an SM and run one after the other.
+// The stage-3 gather's bulk-copy form (one issuing thread per CTA, 4 x 8 KiB
+// ring) over the 68 Llama-7B gathers: 2 CTAs per SM 6590 (6300 at 4; the
+// 16-byte vector form peaks at 6125 with 8 blocks per SM).  Two-stream
+// gather pass (ms, 68 gathers + consumers): the gathers and the consumer
+// must fit on an SM together to overlap at all; bulk gathers at 2 CTAs
+// beside a 7-block consumer gave 12.8 (one-round consumer) and 32.1
+// (64 rounds), against 12.5 and 34.2 for vector gathers at 4 + 4 blocks.
 constexpr int kOccDefault[ZERO_OCC_KINDS] = {
     3,   // ZERO_OCC_FUSED
     8,   // ZERO_OCC_RS
     2,   // ZERO_OCC_ADAM
-    8,   // ZERO_OCC_GATHER
+    2,   // ZERO_OCC_GATHER
     4,   // ZERO_OCC_STREAM
-    4,   // ZERO_OCC_CONSUMER
-    4,   // ZERO_OCC_PREFETCH
+    7,   // ZERO_OCC_CONSUMER
+    2,   // ZERO_OCC_PREFETCH
 };
 std::atomic<int> g_occ[ZERO_OCC_KINDS] = {{0}, {0}, {0}, {0}, {0}, {0}, {0}};
 }  // namespace
