@@ -135,20 +135,26 @@ def measured_hbm_peak():
 
 def kernel_source_hash(kernel: str = "fused_kernel") -> str:
     """Hash of what decides a kernel's DRAM traffic: the device helpers, the
-    kernel's own source text and the occupancy defaults (host code around it
-    does not count)."""
-    csrc = os.path.join(ROOT, "zero_sharded_optimizer_device_gb300", "csrc")
+    kernel's own source text and its occupancy default (host code around it
+    and the other kernels' defaults do not count)."""
+    return _source_hash(_read_csrc("zero_device.cuh"), _read_csrc("zero_rs.cu"), kernel)
+
+
+def _read_csrc(name: str) -> str:
+    with open(os.path.join(ROOT, "zero_sharded_optimizer_device_gb300", "csrc", name)) as f:
+        return f.read()
+
+
+def _source_hash(device_h: str, rs_cu: str, kernel: str) -> str:
     h = hashlib.sha256()
-    with open(os.path.join(csrc, "zero_device.cuh"), "rb") as f:
-        h.update(f.read())
-    with open(os.path.join(csrc, "zero_rs.cu")) as f:
-        text = f.read()
-    start = text.index(f"    {kernel}(")
-    start = text.rindex("template", 0, start)
-    end = text.index("// ------", start)
-    h.update(text[start:end].encode())
-    occ = text.index("constexpr int kOccDefault")
-    h.update(text[occ:text.index("};", occ)].encode())
+    h.update(device_h.encode())
+    start = rs_cu.index(f"    {kernel}(")
+    start = rs_cu.rindex("template", 0, start)
+    end = rs_cu.index("// ------", start)
+    h.update(rs_cu[start:end].encode())
+    occ = rs_cu.index("constexpr int kOccDefault")
+    block = rs_cu[occ:rs_cu.index("};", occ)]
+    h.update(next(line for line in block.splitlines() if "ZERO_OCC_FUSED" in line).encode())
     return h.hexdigest()[:16]
 
 
