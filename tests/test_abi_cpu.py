@@ -87,6 +87,23 @@ def test_planner_matches_oracle_on_edge_cases(numels, n, align, groups):
     _compare_plans(numels, n, align, groups)
 
 
+def test_planner_matches_oracle_on_random_plans():
+    """300 seeded random plans: tensor counts 1-40 (empty tensors included),
+    sizes over six decades, N = 1..64, align 1..128, random layer groups."""
+    import numpy as np
+    rng = np.random.default_rng(2024)
+    for _ in range(300):
+        T = int(rng.integers(1, 41))
+        numels = [0 if rng.random() < 0.05 else int(10 ** rng.uniform(0, 6)) for _ in range(T)]
+        n = int(rng.integers(1, 65))
+        align = int(rng.choice([1, 2, 3, 4, 8, 16, 32, 128]))
+        groups = None
+        if rng.random() < 0.5:
+            g = np.cumsum(rng.random(T) < 0.3)
+            groups = [int(x) for x in (g - g[0])]
+        _compare_plans(numels, n, align, groups)
+
+
 def test_plan_argument_errors():
     for args in [([4], 0, 1), ([4], 65, 1), ([4], 2, 0), ([-1], 2, 1)]:
         with pytest.raises(Z.ZeroError) as e:
