@@ -272,8 +272,8 @@ int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* g
  * dtype: element type of the shard buffers (ZERO_BF16 or ZERO_F32).  When
  * S_g and rank_off(g) are multiples of 16 bytes the N segments move by 1-D
  * bulk copies (TMA) through shared memory, issued by one thread per CTA;
- * their waits are bounded (see zero_async_status).  Otherwise 16-byte vector
- * loads and stores, or single elements where the shards cut vectors. */
+ * their waits are bounded (see zero_async_status).  Otherwise element by
+ * element. */
 int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
                       zero_dtype_t dtype, void* layer_out, zero_stream_t stream);
 

@@ -359,6 +359,37 @@ def test_stage3_outputs_stay_inside_their_buffers(cuda):
         assert bool((b[:G] == -12345.0).all()) and bool((b[-G:] == -12345.0).all()), name
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("n,align", [(16, 16), (4, 8), (5, 4), (3, 3), (7, 1)])
+def test_gather_layer_every_path(cuda, dtype, n, align):
+    """zero_gather_layer on bf16 and fp32 shard buffers, through the bulk-copy
+    form (shard starts and lengths multiples of 16 bytes) and the element
+    form (otherwise): the layer is the concatenation of the owners' shards,
+    bit for bit, with guard bands around it."""
+    import torch
+    rng = np.random.default_rng(1000 * n + align + (7 if dtype == "f32" else 0))
+    numels = [int(x) for x in rng.integers(1, 40_000, 6)]
+    groups = [0, 0, 1, 2, 2, 3]
+    p = O.plan(numels, n, align, groups)
+    Z = pytest.importorskip("zero_sharded_optimizer_device_gb300")
+    zp = Z.zero_plan(numels, n, align, groups)
+    tdt, ndt = (torch.int16, np.uint16) if dtype == "bf16" else (torch.int32, np.uint32)
+    zdt = Z.ZERO_BF16 if dtype == "bf16" else Z.ZERO_F32
+    host = [rng.integers(0, np.iinfo(ndt).max, p.shard_total, dtype=np.uint64).astype(ndt)
+            for _ in range(n)]
+    shards = [torch.from_numpy(h.view(np.int16 if dtype == "bf16" else np.int32)).to(cuda)
+              for h in host]
+    G = 64
+    for gi, g in enumerate(p.groups):
+        buf = torch.full((g.psi_pad + 2 * G,), -7, dtype=tdt, device=cuda)
+        Z.zero_gather_layer(zp, gi, shards, zdt, buf[G:G + g.psi_pad])
+        torch.cuda.synchronize()
+        got = buf.cpu().numpy().view(ndt)
+        want, _, _ = O.gather_layer([h[g.rank_off:g.rank_off + g.shard] for h in host])
+        assert np.array_equal(got[G:G + g.psi_pad], want), (gi, n, align, dtype)
+        assert (buf[:G] == -7).all() and (buf[G + g.psi_pad:] == -7).all(), (gi, "guard")
+
+
 # ------------------------------------------------ full size, sampled windows --
 def test_gpt2_small_full_size_sampled(cuda):
     """The workload the benchmark times (fused zero_step, N=8, bf16 grads),
@@ -383,6 +414,30 @@ def test_gpt2_small_full_size_sampled(cuda):
     for a, b in boundary_windows(P, cuts, 4096):
         r = c.oracle_window(0, (a, b), range(1, w.steps + 1))
         c.check_window(0, (a, b), r, f"gpt2-small [{a},{b})")
+        assert_bf16(bits_of(out[a:b]), r["full"], f"gathered [{a},{b})")
+
+
+def test_gpt2_small_full_size_fp32_gradients_sampled(cuda):
+    """The benchmark's fp32-gradient line (GPT-2-small, N=8, `--grad-dtype
+    f32`: the 32-byte load path of the fused step), 3 steps at full size,
+    sampled windows across every owner boundary and tensor edges."""
+    import torch
+    w = W.GPT2_SMALL
+    c = Case(w.numels, w.n_ranks, w.align, "f32", w.grad_sigma, w.master_sigma, w.seed,
+             host_state=False)
+    Z = c.Z
+    P, S = c.info["psi_pad"], c.groups[0]["shard"]
+    out = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    grads = None
+    for s in range(1, 4):
+        grads = c.grads_dev(0, s, grads)
+        Z.zero_step(c.plan, 0, grads, Z.ZERO_F32, c.master, c.m, c.v, c.hp_dev(s), None, out,
+                    Z.ZERO_BF16)
+    torch.cuda.synchronize()
+    cuts = [k * S for k in range(1, w.n_ranks)] + np.cumsum(w.numels)[:-1].tolist()[::13]
+    for a, b in boundary_windows(P, cuts, 2048):
+        r = c.oracle_window(0, (a, b), range(1, 4))
+        c.check_window(0, (a, b), r, f"gpt2-small fp32 grads [{a},{b})")
         assert_bf16(bits_of(out[a:b]), r["full"], f"gathered [{a},{b})")
 
 

@@ -2,7 +2,7 @@
 //   adam_kernel     Adam over a window of the materialised reduced gradient
 //   cast_kernel     all-gather of the updated parameters into the full buffer
 //   norm_kernel     global gradient norm and clip coefficient
-//   gather_kernel   stage-3 per-layer gather of N rank shards
+//   gather_bulk_kernel / gather_kernel  stage-3 per-layer gather of N rank shards
 //   checksum_kernel consumer of a gathered layer (stands in for its computation)
 //   copy_kernel     16-byte device copy (achievable HBM bandwidth)
 #include "zero_device.cuh"
@@ -182,43 +182,23 @@ cudaError_t launch_norm(const double* partials, int64_t n, float max_norm, float
 }
 
 // ---------------------------------------------------------------------------
-// Stage-3 gather: out[j] = shards[j / S][rank_off + j % S], j < psi_pad.
+// Stage-3 gather, element by element: out[j] = shards[j / S][rank_off + j % S]
+// for j < psi_pad.  Only for shards whose start or length breaks the 16-byte
+// rule of the bulk-copy form below (align < 8 bf16 elements).
 // ---------------------------------------------------------------------------
 template <int ES>
 __global__ void __launch_bounds__(kThreads)
     gather_kernel(RankPtrs shards, GroupK g, int64_t psi_pad, void* __restrict__ out) {
-  constexpr int VW = 16 / ES;  // elements per 16-byte vector
-  const bool vec_ok = ((g.S | g.rank_off) % VW) == 0;
-  if (vec_ok) {
-    const int64_t nv = psi_pad / VW;  // psi_pad is a multiple of S, so of VW
-    int k = 0;                        // a thread's indices only grow: track the owner
-    int64_t next = g.S;               // first element of owner k + 1
-    for (int64_t q = gtid(); q < nv; q += gstride()) {
-      const int64_t j = q * VW;
-      while (j >= next) {
-        ++k;
-        next += g.S;
-      }
-      const int64_t so = g.rank_off + (j - (int64_t)k * g.S);
-      if (!in_extent(k, k + 1, 0, g.n, ZERO_SITE_GATHER_SHARD) ||
-          !in_extent(so, so + VW, g.rank_off, g.rank_off + g.S, ZERO_SITE_GATHER_SHARD) ||
-          !in_extent(j, j + VW, 0, psi_pad, ZERO_SITE_GATHER_OUT))
-        continue;
-      const char* s = static_cast<const char*>(shards.p[k]) + so * ES;
-      st_stream(static_cast<char*>(out) + j * ES, ld_once(s));
-    }
-  } else {
-    for (int64_t j = gtid(); j < psi_pad; j += gstride()) {
-      const int k = owner_of(j, g);
-      const int64_t src = g.rank_off + (j - (int64_t)k * g.S);
-      if (!in_extent(src, src + 1, g.rank_off, g.rank_off + g.S, ZERO_SITE_GATHER_SHARD) ||
-          !in_extent(j, j + 1, 0, psi_pad, ZERO_SITE_GATHER_OUT))
-        continue;
-      if (ES == 2)
-        static_cast<uint16_t*>(out)[j] = static_cast<const uint16_t*>(shards.p[k])[src];
-      else
-        static_cast<uint32_t*>(out)[j] = static_cast<const uint32_t*>(shards.p[k])[src];
-    }
+  for (int64_t j = gtid(); j < psi_pad; j += gstride()) {
+    const int k = owner_of(j, g);
+    const int64_t src = g.rank_off + (j - (int64_t)k * g.S);
+    if (!in_extent(src, src + 1, g.rank_off, g.rank_off + g.S, ZERO_SITE_GATHER_SHARD) ||
+        !in_extent(j, j + 1, 0, psi_pad, ZERO_SITE_GATHER_OUT))
+      continue;
+    if (ES == 2)
+      static_cast<uint16_t*>(out)[j] = static_cast<const uint16_t*>(shards.p[k])[src];
+    else
+      static_cast<uint32_t*>(out)[j] = static_cast<const uint32_t*>(shards.p[k])[src];
   }
 }
 
@@ -232,12 +212,13 @@ __global__ void __launch_bounds__(kThreads)
 // mbarrier wait gives up after ~2 s: the timeout is counted in
 // g_async_timeouts (zero_async_status), the CTA lets the loads it issued
 // land (again bounded) and returns.  Used when every segment start and length
-// is a multiple of 16 bytes; gather_kernel otherwise.
+// is a multiple of 16 bytes; gather_kernel otherwise.  (A 16-byte vector
+// form reached 6125 GB/s on the Llama-7B layers against 6590 for this one.)
 // ---------------------------------------------------------------------------
 constexpr int kBulkChunk = 8192;
 constexpr int kBulkStages = 4;
 constexpr int kBulkThreads = 32;       // one warp per CTA; lane 0 issues
-constexpr int kGatherVecBlocks = 8;    // resident blocks per SM of the vector fallback
+constexpr int kGatherElemBlocks = 8;   // resident blocks per SM of the element fallback
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 static __device__ unsigned long long g_async_timeouts;
@@ -357,16 +338,13 @@ cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& 
         shards, g, elem_bytes, cps, nchunks, static_cast<char*>(out));
     return cudaGetLastError();
   }
-  const int64_t wave = (int64_t)sm_count() * kGatherVecBlocks;
-  if (elem_bytes == 2) {
-    const int64_t want = psi_pad / 8 / kThreads + 1;
-    gather_kernel<2><<<(unsigned)(want < wave ? want : wave), kThreads, 0, st>>>(shards, g,
-                                                                                psi_pad, out);
-  } else {
-    const int64_t want = psi_pad / 4 / kThreads + 1;
-    gather_kernel<4><<<(unsigned)(want < wave ? want : wave), kThreads, 0, st>>>(shards, g,
-                                                                                psi_pad, out);
-  }
+  const int64_t wave = (int64_t)sm_count() * kGatherElemBlocks;
+  const int64_t want = psi_pad / kThreads + 1;
+  const unsigned grid = (unsigned)(want < wave ? want : wave);
+  if (elem_bytes == 2)
+    gather_kernel<2><<<grid, kThreads, 0, st>>>(shards, g, psi_pad, out);
+  else
+    gather_kernel<4><<<grid, kThreads, 0, st>>>(shards, g, psi_pad, out);
   return cudaGetLastError();
 }
 
