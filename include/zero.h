@@ -34,8 +34,11 @@
  *     report argument errors and launch errors only; a later
  *     cudaStreamSynchronize reports execution errors.
  *   - "Device pointer" means any address the GPU can access: device memory,
- *     or pinned host memory mapped into the device address space (cudaHostAlloc
- *     on a unified-addressing system).  Given mapped host buffers for grads or
+ *     pinned host memory mapped into the device address space (cudaHostAlloc
+ *     on a unified-addressing system), or -- where the device reports
+ *     cudaDevAttrPageableMemoryAccess, as a GB300 behind NVLink-C2C does --
+ *     any host memory.  The library does not check; the Python binding
+ *     refuses CPU tensors the device cannot reach.  Given mapped host buffers for grads or
  *     the gathered output, the kernels read and write them over the host link
  *     directly, overlapping the transfer with the step.
  *   - Every device pointer must be 16-byte aligned (ZERO_EALIGN otherwise),

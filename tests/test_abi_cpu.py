@@ -104,6 +104,20 @@ def test_planner_matches_oracle_on_random_plans():
         _compare_plans(numels, n, align, groups)
 
 
+def test_binding_rejects_pageable_cpu_tensors():
+    """A CPU tensor in pageable memory never reaches the library (its address
+    would mean nothing to a kernel); the check runs before any call."""
+    import torch
+    p = Z.zero_plan([100], 2, 16)
+    cpu = torch.zeros(112, dtype=torch.float32)
+    if Z.binding._host_memory_reachable(cpu.data_ptr()):
+        pytest.skip("this system's GPU reads pageable host memory")
+    with pytest.raises(ValueError):
+        Z.zero_all_gather(p, 0, cpu, cpu, Z.ZERO_F32, 0)
+    with pytest.raises(ValueError):
+        Z.zero_gather_layer(p, 0, [cpu, cpu], Z.ZERO_F32, None, 0)
+
+
 def test_plan_argument_errors():
     for args in [([4], 0, 1), ([4], 65, 1), ([4], 2, 0), ([-1], 2, 1)]:
         with pytest.raises(Z.ZeroError) as e:

@@ -166,12 +166,66 @@ def header_functions() -> list[str]:
 
 
 # -------------------------------------------------------------- marshalling --
+class _PointerAttributes(ctypes.Structure):
+    """cudaPointerAttributes as the CUDA 13 runtime lays it out (with its
+    trailing reserved words, which the runtime writes too)."""
+    _fields_ = [("type", ctypes.c_int), ("device", ctypes.c_int),
+                ("devicePointer", c_vp), ("hostPointer", c_vp),
+                ("reserved", ctypes.c_long * 8)]
+
+
+_CUDART = None
+
+
+def _cudart():
+    """The CUDA runtime libzero links against (None when it cannot load)."""
+    global _CUDART
+    if _CUDART is None:
+        try:
+            rt = ctypes.CDLL("libcudart.so.13")
+            rt.cudaPointerGetAttributes.restype = ctypes.c_int
+            rt.cudaPointerGetAttributes.argtypes = [P(_PointerAttributes), c_vp]
+            rt.cudaGetDevice.restype = ctypes.c_int
+            rt.cudaGetDevice.argtypes = [P(ctypes.c_int)]
+            rt.cudaDeviceGetAttribute.restype = ctypes.c_int
+            rt.cudaDeviceGetAttribute.argtypes = [P(ctypes.c_int), ctypes.c_int, ctypes.c_int]
+            _CUDART = rt
+        except OSError:
+            _CUDART = False
+    return _CUDART or None
+
+
+def _host_memory_reachable(addr: int) -> bool:
+    """True when the current device can dereference this host address:
+    page-locked memory mapped at the same address, managed memory, or any
+    host memory on a system whose GPU reads pageable memory directly."""
+    rt = _cudart()
+    if rt is None:
+        return False
+    a = _PointerAttributes()
+    if rt.cudaPointerGetAttributes(ctypes.byref(a), c_vp(addr)) == 0:
+        if a.type == 3 or (a.type == 1 and a.devicePointer == addr):   # managed / mapped host
+            return True
+    dev, flag = ctypes.c_int(), ctypes.c_int()
+    pageable_access = 88                                           # cudaDevAttrPageableMemoryAccess
+    return (rt.cudaGetDevice(ctypes.byref(dev)) == 0 and
+            rt.cudaDeviceGetAttribute(ctypes.byref(flag), pageable_access, dev.value) == 0 and
+            flag.value == 1)
+
+
 def _ptr(x) -> int | None:
+    """Address of a tensor the GPU can reach (a CUDA tensor, or a CPU tensor
+    in host memory the device can dereference); raw integer addresses pass as
+    they are."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
-    return x.data_ptr()
+    addr = x.data_ptr()
+    if not x.is_cuda and not (x.is_pinned() or _host_memory_reachable(addr)):
+        raise ValueError("a CPU tensor in pageable host memory is not device-accessible here: "
+                         "use a CUDA tensor or page-locked (pinned) host memory")
+    return addr
 
 
 def _stream(s) -> int | None:
