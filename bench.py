@@ -622,9 +622,11 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
 # ------------------------------------------- stage-3 gather granularity sweep --
 def regroup(w, per: str):
     """Layer-group list of the stage-3 workload at another granularity:
-    'tensor' (per-parameter partitioning: every tensor its own group),
-    'layer' (the workload's groups) or 'k-layers' (k consecutive groups)."""
-    if per == "tensor":
+    'tensor' (per-parameter partitioning: every tensor its own group; also
+    'tensor-coalesced', the same plan gathered one layer's tensors per
+    launch), 'layer' (the workload's groups) or 'k-layers' (k consecutive
+    groups)."""
+    if per.startswith("tensor"):
         return list(range(len(w.numels)))
     if per == "layer":
         return list(w.groups)
@@ -645,7 +647,7 @@ def bench_gather_sweep(w, steps: int, dist: Dist, only=None) -> dict:
     N = w.n_ranks
     sa = torch.cuda.current_stream(dev)
     res = {}
-    for per in ("tensor", "layer", "2-layers", "4-layers"):
+    for per in ("tensor", "tensor-coalesced", "layer", "2-layers", "4-layers"):
         if only and per != only:
             continue
         groups_of = regroup(w, per)
@@ -657,12 +659,31 @@ def bench_gather_sweep(w, steps: int, dist: Dist, only=None) -> dict:
         for r in range(N):
             synth.fill_tensor(shards[r], w.seed, synth.MASTER, 0, r, 0, w.master_sigma,
                               info["shard_total"])
-        gmax = max(g["psi_pad"] for g in groups)
-        bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(2)]
-        order = list(range(len(groups))) + list(reversed(range(len(groups))))
-        calls = [lambda j=j, gi=gi: Z.zero_gather_layer(plan, gi, shards, Z.ZERO_BF16,
-                                                        bufs[j % 2], sa)
-                 for j, gi in enumerate(order)]
+        if per == "tensor-coalesced":
+            # one launch per layer: that layer's tensors, each into its own
+            # 16-byte-aligned slice of the layer's buffer
+            layers = [[t for t, g in enumerate(w.groups) if g == L] for L in sorted(set(w.groups))]
+            spans = []
+            for ts in layers:
+                offs, o = [], 0
+                for t in ts:
+                    offs.append(o)
+                    o += -(-groups[t]["psi_pad"] // 8) * 8
+                spans.append((ts, offs, o))
+            gmax = max(o for _, _, o in spans)
+            bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+            order = list(range(len(layers))) + list(reversed(range(len(layers))))
+            calls = [lambda j=j, L=L: Z.zero_gather_groups(
+                plan, spans[L][0], shards, Z.ZERO_BF16,
+                [bufs[j % 2][o:] for o in spans[L][1]], sa)
+                for j, L in enumerate(order)]
+        else:
+            gmax = max(g["psi_pad"] for g in groups)
+            bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+            order = list(range(len(groups))) + list(reversed(range(len(groups))))
+            calls = [lambda j=j, gi=gi: Z.zero_gather_layer(plan, gi, shards, Z.ZERO_BF16,
+                                                            bufs[j % 2], sa)
+                     for j, gi in enumerate(order)]
         _timed_launches(sa, calls)                     # warm-up
         ms = statistics.fmean(sum(_timed_launches(sa, calls)) for _ in range(steps))
         elems = 2 * sum(g["psi_pad"] for g in groups)
@@ -821,7 +842,7 @@ def main(argv=None):
     ap.add_argument("--gather-sweep", action="store_true",
                     help="stage-3 workload: gather bandwidth at several partition granularities")
     ap.add_argument("--gather-granularity", default=None,
-                    choices=["tensor", "layer", "2-layers", "4-layers"],
+                    choices=["tensor", "tensor-coalesced", "layer", "2-layers", "4-layers"],
                     help="with --gather-sweep: only this granularity")
     args = ap.parse_args(argv)
     from synth import workloads as W

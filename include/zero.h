@@ -280,6 +280,20 @@ int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* g
 int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
                       zero_dtype_t dtype, void* layer_out, zero_stream_t stream);
 
+/* zero_gather_groups (stage 3): zero_gather_layer for k groups at once:
+ * layer_outs[i] receives group groups[i] (1 <= k <= ZERO_MAX_COALESCE; a
+ * group may repeat).  Groups whose shards meet the 16-byte rule share one
+ * bulk-copy launch; the others are gathered element by element, one launch
+ * each.  Made for per-parameter partitioning, where every tensor is its own
+ * group and a module's tensors are needed together ("ZeRO Optimizer",
+ * "Implementation Strategy": a layer's parameters are gathered before use):
+ * one launch instead of one per tensor, each tensor still in its own buffer.
+ * Errors: EINVAL, EALIGN, ERANGE (group id), EDTYPE, ECUDA. */
+#define ZERO_MAX_COALESCE 64
+int zero_gather_groups(const zero_plan_t* plan, const int32_t* groups, int32_t k,
+                       const void* const* shards, zero_dtype_t dtype, void* const* layer_outs,
+                       zero_stream_t stream);
+
 /* zero_stage3_gather_pass (stage 3) ["ZeRO Optimizer", "Implementation
  * Strategy": gather a layer's parameters just before use, discard after, in
  * forward and backward; "Communication Optimization": hide the gathering

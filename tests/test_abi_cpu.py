@@ -177,6 +177,13 @@ def test_device_call_argument_errors_return_before_any_launch():
     assert status(Z.zero_adam_shard, p, 0, A, A, A, A, hp, None, 0, 200, None) == Z.ZERO_ERANGE
     assert status(Z.zero_all_gather, p, 3, A, A) == Z.ZERO_ERANGE
     assert status(Z.zero_gather_layer, p, 0, good, Z.ZERO_BF16, A + 1) == Z.ZERO_EALIGN
+    assert status(Z.zero_gather_groups, p, [0], good, Z.ZERO_BF16, [A + 2]) == Z.ZERO_EALIGN
+    assert status(Z.zero_gather_groups, p, [0, 1], good, Z.ZERO_BF16, [A, A]) == Z.ZERO_ERANGE
+    assert status(Z.zero_gather_groups, p, [], good, Z.ZERO_BF16, []) == Z.ZERO_EINVAL
+    assert status(Z.zero_gather_groups, p, [0] * 65, good, Z.ZERO_BF16, [A] * 65) == \
+        Z.ZERO_EINVAL
+    assert status(Z.zero_gather_groups, p, [0], good, 5, [A]) == Z.ZERO_EDTYPE
+    assert status(Z.zero_gather_groups, p, [0], good, Z.ZERO_BF16, [0]) == Z.ZERO_EINVAL
     assert status(Z.zero_grad_norm, A, 4, 0.0, None, None) == Z.ZERO_EINVAL
     assert status(Z.zero_layer_checksum, A, 10, 1, A + 4) == Z.ZERO_EALIGN
     assert status(Z.zero_layer_checksum, A, 10, 0, A) == Z.ZERO_EINVAL

@@ -390,6 +390,41 @@ def test_gather_layer_every_path(cuda, dtype, n, align):
         assert (buf[:G] == -7).all() and (buf[G + g.psi_pad:] == -7).all(), (gi, "guard")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("n,align", [(16, 16), (8, 1), (5, 3)])
+def test_gather_groups_per_parameter(cuda, dtype, n, align):
+    """Per-parameter partitioning (every tensor its own group): zero_gather_groups
+    over a module's tensors, in random subsets and orders with repeats,
+    equals each tensor's own gather, bit for bit; mixed bulk-copy and
+    element-wise groups in one call; guard bands around every output."""
+    import torch
+    rng = np.random.default_rng(77 * n + align + (5 if dtype == "f32" else 0))
+    numels = [int(x) for x in rng.integers(1, 30_000, 12)] + [0, 7]
+    groups = list(range(len(numels)))
+    p = O.plan(numels, n, align, groups)
+    Z = pytest.importorskip("zero_sharded_optimizer_device_gb300")
+    zp = Z.zero_plan(numels, n, align, groups)
+    tdt, ndt = (torch.int16, np.uint16) if dtype == "bf16" else (torch.int32, np.uint32)
+    zdt = Z.ZERO_BF16 if dtype == "bf16" else Z.ZERO_F32
+    host = [rng.integers(0, np.iinfo(ndt).max, p.shard_total, dtype=np.uint64).astype(ndt)
+            for _ in range(n)]
+    shards = [torch.from_numpy(h.view(np.int16 if dtype == "bf16" else np.int32)).to(cuda)
+              for h in host]
+    G = 64
+    for trial in range(4):
+        pick = [int(x) for x in rng.integers(0, len(groups), int(rng.integers(1, 20)))]
+        bufs = [torch.full((p.groups[g].psi_pad + 2 * G,), -7, dtype=tdt, device=cuda)
+                for g in pick]
+        Z.zero_gather_groups(zp, pick, shards, zdt, [b[G:] for b in bufs])
+        torch.cuda.synchronize()
+        for g, b in zip(pick, bufs):
+            gi = p.groups[g]
+            got = b.cpu().numpy().view(ndt)
+            want, _, _ = O.gather_layer([h[gi.rank_off:gi.rank_off + gi.shard] for h in host])
+            assert np.array_equal(got[G:G + gi.psi_pad], want), (trial, g)
+            assert (b[:G] == -7).all() and (b[G + gi.psi_pad:] == -7).all(), (trial, g)
+
+
 # ------------------------------------------------ full size, sampled windows --
 def test_gpt2_small_full_size_sampled(cuda):
     """The workload the benchmark times (fused zero_step, N=8, bf16 grads),

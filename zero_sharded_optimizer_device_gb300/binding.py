@@ -35,6 +35,7 @@ ZERO_MAX_POLLS = 10_000_000
 ZERO_OCC_FUSED, ZERO_OCC_RS, ZERO_OCC_ADAM, ZERO_OCC_GATHER, ZERO_OCC_STREAM, \
     ZERO_OCC_CONSUMER, ZERO_OCC_PREFETCH = range(7)
 ZERO_MAX_CONSUMER_ROUNDS = 4096
+ZERO_MAX_COALESCE = 64
 
 _NAMES = {0: "ZERO_OK", -1: "ZERO_EINVAL", -2: "ZERO_EALIGN", -3: "ZERO_ERANGE",
           -4: "ZERO_EDTYPE", -5: "ZERO_ENOMEM", -6: "ZERO_ECUDA", -7: "ZERO_ETIMEOUT"}
@@ -124,6 +125,7 @@ _SIGS = {
     "zero_step_group": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp,
                                 P(zero_adam_t), c_vp, P(c_vp), c_vp]),
     "zero_gather_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
+    "zero_gather_groups": (c_i32, [c_vp, P(c_i32), c_i32, P(c_vp), c_i32, P(c_vp), c_vp]),
     "zero_layer_checksum": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp]),
     "zero_stage3_gather_pass": (c_i32, [c_vp, P(c_i32), c_i32, P(c_vp), P(c_vp), c_i64, c_vp,
                                         c_i32, c_vp, c_vp]),
@@ -397,6 +399,13 @@ def zero_step_group(plan, group, grads, gdtype, master, m, v, hp, d_coef, shards
 def zero_gather_layer(plan, group, shards, dtype, layer_out, stream=None) -> None:
     _check(_lib().zero_gather_layer(plan, group, _ptr_array(shards), dtype, _ptr(layer_out),
                                     _stream(stream)), "zero_gather_layer")
+
+
+def zero_gather_groups(plan, groups, shards, dtype, layer_outs, stream=None) -> None:
+    arr = (c_i32 * max(1, len(groups)))(*[int(g) for g in groups])
+    _check(_lib().zero_gather_groups(plan, arr, len(groups), _ptr_array(shards), dtype,
+                                     _ptr_array(layer_outs), _stream(stream)),
+           "zero_gather_groups")
 
 
 def zero_stage3_gather_pass(plan, order, shards, layer_bufs, buf_elems, d_sums,

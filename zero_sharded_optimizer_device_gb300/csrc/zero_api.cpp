@@ -321,6 +321,36 @@ extern "C" int zero_gather_layer(const zero_plan_t* plan, int32_t group, const v
                                        layer_out, ZERO_OCC_GATHER, (cudaStream_t)stream));
 }
 
+extern "C" int zero_gather_groups(const zero_plan_t* plan, const int32_t* groups, int32_t k,
+                                  const void* const* shards, zero_dtype_t dtype,
+                                  void* const* layer_outs, zero_stream_t stream) {
+  NvtxRange nvtx("zero_gather_groups");
+  if (!plan || !groups || !layer_outs || k < 1 || k > ZERO_MAX_COALESCE) return ZERO_EINVAL;
+  if (!dtype_ok(dtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_rank_ptrs(plan, shards));
+  for (int32_t i = 0; i < k; ++i) {
+    ZERO_TRY(check_group(plan, groups[i]));
+    ZERO_TRY(check_buf(layer_outs[i]));
+  }
+  const int es = dtype == ZERO_BF16 ? 2 : 4;
+  const zk::RankPtrs src = rank_ptrs(plan, shards);
+  zk::BulkGroups bg{};
+  bg.es = es;
+  bg.n = plan->n_ranks;
+  cudaError_t e = cudaSuccess;
+  for (int32_t i = 0; i < k && e == cudaSuccess; ++i) {
+    const zero_group_info_t& g = plan->groups[groups[i]];
+    if (zk::bulk_eligible(g.shard, g.rank_off, es))
+      zk::bulk_add(bg, g.shard, g.rank_off, layer_outs[i]);
+    else
+      e = zk::launch_gather(src, es, group_k(plan, groups[i]), g.psi_pad, layer_outs[i],
+                            ZERO_OCC_GATHER, (cudaStream_t)stream);
+  }
+  if (e == cudaSuccess && bg.ng > 0)
+    e = zk::launch_gather_bulk(src, bg, ZERO_OCC_GATHER, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
 extern "C" int zero_layer_checksum(const void* layer, int64_t n, int32_t rounds,
                                    uint64_t* d_out, zero_stream_t stream) {
   NvtxRange nvtx("zero_layer_checksum");

@@ -97,6 +97,22 @@ cudaError_t launch_norm(const double* partials, int64_t n, float max_norm, float
 cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
                           int64_t psi_pad, void* out, int occ_kind, cudaStream_t st);
 
+// Groups gathered by one bulk-copy launch (kernel parameter, by value).
+struct BulkGroups {
+  int ng;  // groups in use
+  int es;  // element bytes
+  int n;   // ranks
+  int64_t first[ZERO_MAX_COALESCE + 1];  // within one owner: first piece of each group
+  int64_t S[ZERO_MAX_COALESCE], rank_off[ZERO_MAX_COALESCE];
+  char* out[ZERO_MAX_COALESCE];
+};
+// Shard start and length both multiples of 16 bytes (the bulk copies' rule).
+bool bulk_eligible(int64_t S, int64_t rank_off, int elem_bytes);
+// Append a group (bg.es and bg.n set, bg.ng < ZERO_MAX_COALESCE).
+void bulk_add(BulkGroups& bg, int64_t S, int64_t rank_off, void* out);
+cudaError_t launch_gather_bulk(const RankPtrs& shards, const BulkGroups& bg, int occ_kind,
+                               cudaStream_t st);
+
 cudaError_t launch_checksum(const void* layer, int64_t n, int rounds, uint64_t* out,
                             cudaStream_t st);
 

@@ -248,9 +248,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// The pieces of one launch are numbered owner by owner: owner k's pieces of
+// all the launch's groups come before owner k+1's, so the CTAs stream one
+// rank's shard buffer at a time, as for a single group.  Within owner k,
+// group i's segment is pieces [first[i], first[i+1]).
 __global__ void __launch_bounds__(kBulkThreads)
-    gather_bulk_kernel(RankPtrs shards, GroupK g, int es, int64_t cps, int64_t nchunks,
-                       char* __restrict__ out) {
+    gather_bulk_kernel(RankPtrs shards, BulkGroups bg) {
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ __align__(8) uint64_t full[kBulkStages];
   if (threadIdx.x != 0) return;
@@ -258,23 +261,33 @@ __global__ void __launch_bounds__(kBulkThreads)
   for (int s = 0; s < kBulkStages; ++s)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s));
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  const int64_t G = gridDim.x, b = blockIdx.x;
+  const int64_t G = gridDim.x, b = blockIdx.x, per_owner = bg.first[bg.ng];
+  const int64_t nchunks = per_owner * bg.n;
   const int64_t niter = b < nchunks ? (nchunks - b + G - 1) / G : 0;
-  const int64_t segb = g.S * es;
+  const int es = bg.es;
   // piece i of this CTA: source, destination, bytes (false: outside its
   // extent, which only the checked build can report)
   auto piece = [&](int64_t i, const char*& src, char*& dst, uint32_t& bytes) {
     const int64_t c = b + i * G;
-    const int k = (int)(c / cps);
-    const int64_t off = (c % cps) * kBulkChunk;
-    const int64_t rem = segb - off;
+    const int k = (int)(c / per_owner);
+    const int64_t co = c - (int64_t)k * per_owner;  // piece within owner k
+    int lo = 0, hi = bg.ng - 1;  // the last group whose first piece is <= co
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (bg.first[mid] <= co) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t S = bg.S[lo], ro = bg.rank_off[lo];
+    const int64_t off = (co - bg.first[lo]) * kBulkChunk;
+    const int64_t rem = S * es - off;
     bytes = (uint32_t)(rem < kBulkChunk ? rem : kBulkChunk);
-    const int64_t so = g.rank_off + off / es, j = (int64_t)k * g.S + off / es, len = bytes / es;
+    const int64_t so = ro + off / es, j = (int64_t)k * S + off / es, len = bytes / es;
     src = static_cast<const char*>(shards.p[k]) + so * es;
-    dst = out + j * es;
-    return in_extent(k, k + 1, 0, g.n, ZERO_SITE_GATHER_SHARD) &&
-           in_extent(so, so + len, g.rank_off, g.rank_off + g.S, ZERO_SITE_GATHER_SHARD) &&
-           in_extent(j, j + len, 0, (int64_t)g.n * g.S, ZERO_SITE_GATHER_OUT);
+    dst = bg.out[lo] + j * es;
+    return in_extent(co, co + 1, bg.first[lo], bg.first[lo + 1], ZERO_SITE_GATHER_OUT) &&
+           in_extent(k, k + 1, 0, bg.n, ZERO_SITE_GATHER_SHARD) &&
+           in_extent(so, so + len, ro, ro + S, ZERO_SITE_GATHER_SHARD) &&
+           in_extent(j, j + len, 0, (int64_t)bg.n * S, ZERO_SITE_GATHER_OUT);
   };
   auto load = [&](int64_t i) {
     const uint32_t bar = bar0 + 8 * (uint32_t)(i % kBulkStages);
@@ -326,17 +339,38 @@ __global__ void __launch_bounds__(kBulkThreads)
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+bool bulk_eligible(int64_t S, int64_t rank_off, int elem_bytes) {
+  return (S * elem_bytes) % 16 == 0 && (rank_off * elem_bytes) % 16 == 0;
+}
+
+void bulk_add(BulkGroups& bg, int64_t S, int64_t rank_off, void* out) {
+  const int i = bg.ng++;
+  const int64_t cps = S > 0 ? (S * bg.es + kBulkChunk - 1) / kBulkChunk : 0;
+  bg.S[i] = S;
+  bg.rank_off[i] = rank_off;
+  bg.out[i] = static_cast<char*>(out);
+  bg.first[i + 1] = bg.first[i] + cps;
+}
+
+cudaError_t launch_gather_bulk(const RankPtrs& shards, const BulkGroups& bg, int occ_kind,
+                               cudaStream_t st) {
+  const int64_t nchunks = bg.first[bg.ng] * bg.n;
+  if (nchunks <= 0) return cudaSuccess;
+  int64_t grid = (int64_t)sm_count() * occupancy_cap(occ_kind);
+  if (grid > nchunks) grid = nchunks;
+  gather_bulk_kernel<<<(unsigned)grid, kBulkThreads, kBulkStages * kBulkChunk, st>>>(shards, bg);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
                           int64_t psi_pad, void* out, int occ_kind, cudaStream_t st) {
   if (psi_pad <= 0) return cudaSuccess;
-  const int64_t segb = g.S * elem_bytes;
-  if (segb % 16 == 0 && (g.rank_off * elem_bytes) % 16 == 0) {
-    const int64_t cps = (segb + kBulkChunk - 1) / kBulkChunk, nchunks = g.n * cps;
-    int64_t grid = (int64_t)sm_count() * occupancy_cap(occ_kind);
-    if (grid > nchunks) grid = nchunks;
-    gather_bulk_kernel<<<(unsigned)grid, kBulkThreads, kBulkStages * kBulkChunk, st>>>(
-        shards, g, elem_bytes, cps, nchunks, static_cast<char*>(out));
-    return cudaGetLastError();
+  if (bulk_eligible(g.S, g.rank_off, elem_bytes)) {
+    BulkGroups bg{};
+    bg.es = elem_bytes;
+    bg.n = g.n;
+    bulk_add(bg, g.S, g.rank_off, out);
+    return launch_gather_bulk(shards, bg, occ_kind, st);
   }
   const int64_t wave = (int64_t)sm_count() * kGatherElemBlocks;
   const int64_t want = psi_pad / kThreads + 1;
