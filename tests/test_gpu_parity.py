@@ -48,6 +48,49 @@ def test_tiny_fused_three_steps(cuda, out_dtype):
     assert not c.master[w.psi:].any().item()
 
 
+def test_plain_c_program_drives_the_step(cuda, tmp_path):
+    """A C99 program with its own cudaMalloc'd buffers (no Python framework
+    between it and the ABI) runs three fused steps of the tiny workload; its
+    master, m, v and gathered parameters equal the oracle's, bit for bit."""
+    import os
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    lib_dir = os.path.join(root, "zero_sharded_optimizer_device_gb300")
+    cuda_home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    exe = str(tmp_path / "c_abi_step")
+    # C11 rather than pedantic C99: the CUDA runtime header uses anonymous unions
+    cc = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror",
+                         "-I", os.path.join(root, "include"), "-I", f"{cuda_home}/include",
+                         os.path.join(root, "tests", "c_abi_step.c"), "-L", lib_dir, "-lzero",
+                         "-L", f"{cuda_home}/lib64", "-lcudart", f"-Wl,-rpath,{lib_dir}",
+                         f"-Wl,-rpath,{cuda_home}/lib64", "-o", exe],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    w = W.TINY
+    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed)
+    P, N, steps = c.info["psi_pad"], w.n_ranks, 3
+    grads = c.grads_host(0, 1)                 # the same gradients every step
+    header = (np.array([N, steps], np.int32).tobytes() + np.array([P], np.int64).tobytes() +
+              np.array([len(w.numels)], np.int32).tobytes() +
+              np.array(w.numels, np.int64).tobytes())
+    inp = tmp_path / "in.bin"
+    inp.write_bytes(header + b"".join(g.astype(np.float32).tobytes() for g in grads) +
+                    c.h_master.astype(np.float32).tobytes())
+    outp = tmp_path / "out.bin"
+    run = subprocess.run([exe, str(inp), str(outp)], capture_output=True, text=True)
+    assert run.returncode == 0, (run.returncode, run.stderr)
+    raw = outp.read_bytes()
+    got = [np.frombuffer(raw[i * 4 * P:(i + 1) * 4 * P], np.float32) for i in range(3)]
+    got_out = np.frombuffer(raw[12 * P:], np.uint16)
+    master, m, v = c.h_master.copy(), c.h_m.copy(), c.h_v.copy()
+    for s in range(1, steps + 1):
+        r = O.zero_step(grads, master, m, v, c.groups[0]["shard"], s, c.hp)
+        master, m, v = r["master"], r["m"], r["v"]
+    for g, want, what in zip(got, (master, m, v), ("master", "m", "v")):
+        assert_close_f32(g, want, f"C program {what}")
+    assert_bf16(got_out, r["full"], "C program gathered")
+
+
 def test_tiny_unfused_chain(cuda):
     import torch
     w = W.TINY
