@@ -468,6 +468,35 @@ def test_gather_groups_per_parameter(cuda, dtype, n, align):
             assert (b[:G] == -7).all() and (b[G + gi.psi_pad:] == -7).all(), (trial, g)
 
 
+def test_gather_groups_and_consumer_at_their_limits(cuda):
+    """ZERO_MAX_COALESCE groups in one zero_gather_groups call, and the
+    consumer at ZERO_MAX_CONSUMER_ROUNDS rounds, against the oracle."""
+    import torch
+    Z = pytest.importorskip("zero_sharded_optimizer_device_gb300")
+    rng = np.random.default_rng(64)
+    n, k = 4, Z.ZERO_MAX_COALESCE
+    numels = [int(x) for x in rng.integers(1, 3000, k + 6)]
+    groups = list(range(len(numels)))
+    p = O.plan(numels, n, 16, groups)
+    zp = Z.zero_plan(numels, n, 16, groups)
+    host = [rng.integers(0, 1 << 16, p.shard_total, dtype=np.uint64).astype(np.uint16)
+            for _ in range(n)]
+    shards = [torch.from_numpy(h.view(np.int16)).to(cuda) for h in host]
+    pick = [int(x) for x in rng.permutation(len(numels))[:k]]
+    outs = [torch.empty(p.groups[g].psi_pad, dtype=torch.int16, device=cuda) for g in pick]
+    Z.zero_gather_groups(zp, pick, shards, Z.ZERO_BF16, outs)
+    sums = torch.zeros(1, dtype=torch.int64, device=cuda)
+    Z.zero_layer_checksum(outs[0], p.groups[pick[0]].psi_pad, Z.ZERO_MAX_CONSUMER_ROUNDS, sums)
+    torch.cuda.synchronize()
+    for g, o in zip(pick, outs):
+        gi = p.groups[g]
+        want, _, _ = O.gather_layer([h[gi.rank_off:gi.rank_off + gi.shard] for h in host])
+        assert np.array_equal(o.cpu().numpy().view(np.uint16), want), g
+    want0, _, _ = O.gather_layer([h[p.groups[pick[0]].rank_off:p.groups[pick[0]].rank_off +
+                                    p.groups[pick[0]].shard] for h in host])
+    assert int(sums.item()) % (1 << 64) == O.layer_checksum(want0, Z.ZERO_MAX_CONSUMER_ROUNDS)
+
+
 # ------------------------------------------------ full size, sampled windows --
 def test_gpt2_small_full_size_sampled(cuda):
     """The workload the benchmark times (fused zero_step, N=8, bf16 grads),
