@@ -118,6 +118,33 @@ def test_binding_rejects_pageable_cpu_tensors():
         Z.zero_gather_layer(p, 0, [cpu, cpu], Z.ZERO_F32, None, 0)
 
 
+def test_planner_from_several_host_threads():
+    """Plans are built and queried from 8 host threads at once (the library
+    keeps no shared mutable planner state); every thread sees the oracle's map."""
+    import threading
+    w = W.GPT2_SMALL
+    o = O.plan(w.numels, w.n_ranks, w.align)
+    errors = []
+
+    def worker():
+        try:
+            for _ in range(20):
+                p = Z.zero_plan(w.numels, w.n_ranks, w.align)
+                info = Z.zero_plan_info(p)
+                assert (info["psi_pad"], info["shard_total"]) == (o.psi_pad, o.shard_total)
+                for r in (0, w.n_ranks - 1):
+                    assert Z.zero_plan_segments(p, r) == o.segments(r)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker) for _ in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[0]
+
+
 def test_plan_argument_errors():
     for args in [([4], 0, 1), ([4], 65, 1), ([4], 2, 0), ([-1], 2, 1)]:
         with pytest.raises(Z.ZeroError) as e:
