@@ -243,6 +243,30 @@ int zero_adam_shard(const zero_plan_t* plan, int32_t group, float* master, float
                     int64_t begin, int64_t end, void* out, zero_dtype_t out_dtype,
                     zero_stream_t stream);
 
+/* zero_step_clipped: the step with gradient clipping of group g in one call
+ * (the path of a run that clips: the reduced gradient has to exist before
+ * its global norm does).  The plain step zero_step cannot clip by the norm
+ * of the step's own gradient, since it never materialises the reduced
+ * gradient; this call strings the unfused calls together on `stream`, with
+ * results identical, bit for bit, to making them one by one:
+ *   zero_reduce_scatter over windows [a, a+bucket) of the group, writing
+ *     `reduced` and each window's norm partials into consecutive slices of
+ *     `partials` (scale hp->grad_scale);
+ *   zero_grad_norm over all of them with max_norm -> *d_norm (may be NULL)
+ *     and *d_coef (required);
+ *   zero_adam_shard over chunks [a, a+chunk) with d_coef, writing full_out
+ *     (may be NULL) in out_dtype.
+ * partials: caller-owned fp64 scratch of n_partials >= the count
+ * zero_step_clipped_partials reports (ERANGE otherwise).  bucket, chunk >= 1.
+ * Errors: EINVAL, EALIGN, ERANGE, EDTYPE, ECUDA. */
+int zero_step_clipped_partials(const zero_plan_t* plan, int32_t group, zero_dtype_t gdtype,
+                               int64_t bucket, int64_t* n_partials);
+int zero_step_clipped(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                      zero_dtype_t gdtype, float* reduced, float* master, float* m, float* v,
+                      const zero_adam_t* hp, float max_norm, int64_t bucket, int64_t chunk,
+                      double* partials, int64_t n_partials, float* d_norm, float* d_coef,
+                      void* full_out, zero_dtype_t out_dtype, zero_stream_t stream);
+
 /* zero_all_gather [P1 "Problem"; P3 all-gather]: full_out[f] = cast(
  * master[f]) for every element of group g (g = -1: all groups), i.e. every
  * owner's updated shard lands in the one full flat parameter buffer all

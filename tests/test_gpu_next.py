@@ -389,6 +389,64 @@ def test_cuda_graph_of_the_bucketed_clip_pipeline(cuda):
     assert torch.equal(ba[3], bb[3]) and torch.equal(ba[2], bb[2])
 
 
+def test_step_clipped_equals_the_calls_it_strings_together(cuda):
+    """zero_step_clipped (bucketed reduce-scatter with norm partials, norm,
+    clip, chunked Adam, cast in one call) equals the same calls made one by
+    one, bit for bit, over two steps of the Llama-1.4B mini with heavy tails
+    (clip active); its argument checks return their codes."""
+    import torch
+    w = W.mini(W.LLAMA_1_4B, scale=1024)
+    a, b = (Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma,
+                 w.seed, heavy_tail=True, host_state=False) for _ in range(2))
+    Z = a.Z
+    P = a.info["psi_pad"]
+    bucket, chunk = 100_003, 400_001
+    windows = [(x, min(P, x + bucket)) for x in range(0, P, bucket)]
+    npart = [Z.zero_rs_partials(a.plan, Z.ZERO_BF16, hi - lo) for lo, hi in windows]
+    total = Z.zero_step_clipped_partials(b.plan, 0, Z.ZERO_BF16, bucket)
+    assert total == sum(npart)
+
+    def bufs():
+        return (torch.empty(P, dtype=torch.float32, device=cuda),
+                torch.zeros(total, dtype=torch.float64, device=cuda),
+                torch.zeros(1, dtype=torch.float32, device=cuda),
+                torch.zeros(1, dtype=torch.float32, device=cuda),
+                torch.empty(P, dtype=torch.bfloat16, device=cuda))
+
+    ra, pa, na, ca, oa = bufs()
+    rb, pb, nb, cb, ob = bufs()
+    for s in (1, 2):
+        grads = a.grads_dev(0, s)
+        off = 0
+        for (lo, hi), k in zip(windows, npart):
+            Z.zero_reduce_scatter(a.plan, 0, grads, Z.ZERO_BF16, ra, lo, hi, 1.0 / a.n,
+                                  pa[off:off + k])
+            off += k
+        Z.zero_grad_norm(pa, off, 1.0, na, ca)
+        for lo in range(0, P, chunk):
+            Z.zero_adam_shard(a.plan, 0, a.master, a.m, a.v, ra, a.hp_dev(s), ca, lo,
+                              min(P, lo + chunk), oa, Z.ZERO_BF16)
+        Z.zero_step_clipped(b.plan, 0, grads, Z.ZERO_BF16, rb, b.master, b.m, b.v, b.hp_dev(s),
+                            1.0, bucket, chunk, pb, total, nb, cb, ob, Z.ZERO_BF16)
+        torch.cuda.synchronize()
+        assert float(ca.item()) < 1.0                      # the clip is active
+        for x, y, what in ((a.master, b.master, "master"), (a.m, b.m, "m"), (a.v, b.v, "v"),
+                           (oa, ob, "out"), (ra, rb, "reduced"), (na, nb, "norm"),
+                           (ca, cb, "coef")):
+            assert torch.equal(x, y), (s, what)
+    E = Z.ZeroError
+    g = b.grads_dev(0, 3)
+    for kw, status in [(dict(n_partials=total - 1), Z.ZERO_ERANGE), (dict(bucket=0), Z.ZERO_EINVAL),
+                       (dict(d_coef=None), Z.ZERO_EINVAL), (dict(max_norm=0.0), Z.ZERO_EINVAL)]:
+        args = dict(n_partials=total, bucket=bucket, d_coef=cb, max_norm=1.0)
+        args.update(kw)
+        with pytest.raises(E) as e:
+            Z.zero_step_clipped(b.plan, 0, g, Z.ZERO_BF16, rb, b.master, b.m, b.v, b.hp_dev(3),
+                                args["max_norm"], args["bucket"], chunk, pb, args["n_partials"],
+                                nb, args["d_coef"], ob, Z.ZERO_BF16)
+        assert e.value.status == status
+
+
 def test_fp32_gradient_load_paths_agree(cuda):
     """fp32 gradient buffers that are all 32-byte aligned take one 32-byte
     load per thread, others two 16-byte loads: identical results, device and

@@ -120,6 +120,10 @@ _SIGS = {
     "zero_adam_shard": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, P(zero_adam_t), c_vp,
                                 c_i64, c_i64, c_vp, c_i32, c_vp]),
     "zero_all_gather": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_i32, c_vp]),
+    "zero_step_clipped_partials": (c_i32, [c_vp, c_i32, c_i32, c_i64, P(c_i64)]),
+    "zero_step_clipped": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp, c_vp,
+                                  P(zero_adam_t), ctypes.c_float, c_i64, c_i64, c_vp, c_i64,
+                                  c_vp, c_vp, c_vp, c_i32, c_vp]),
     "zero_step": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp, P(zero_adam_t), c_vp,
                           c_vp, c_i32, c_vp]),
     "zero_step_group": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp,
@@ -375,6 +379,23 @@ def zero_adam_shard(plan, group, master, m, v, reduced, hp, d_coef, begin, end, 
     _check(_lib().zero_adam_shard(plan, group, _ptr(master), _ptr(m), _ptr(v), _ptr(reduced),
                                   ctypes.byref(hp), _ptr(d_coef), begin, end, _ptr(out),
                                   out_dtype, _stream(stream)), "zero_adam_shard")
+
+
+def zero_step_clipped_partials(plan, group, gdtype, bucket) -> int:
+    n = c_i64()
+    _check(_lib().zero_step_clipped_partials(plan, group, gdtype, bucket, ctypes.byref(n)),
+           "zero_step_clipped_partials")
+    return n.value
+
+
+def zero_step_clipped(plan, group, grads, gdtype, reduced, master, m, v, hp, max_norm, bucket,
+                      chunk, partials, n_partials, d_norm, d_coef, full_out,
+                      out_dtype=ZERO_BF16, stream=None) -> None:
+    _check(_lib().zero_step_clipped(plan, group, _ptr_array(grads), gdtype, _ptr(reduced),
+                                    _ptr(master), _ptr(m), _ptr(v), ctypes.byref(hp), max_norm,
+                                    bucket, chunk, _ptr(partials), n_partials, _ptr(d_norm),
+                                    _ptr(d_coef), _ptr(full_out), out_dtype, _stream(stream)),
+           "zero_step_clipped")
 
 
 def zero_all_gather(plan, group, master, full_out, out_dtype=ZERO_BF16, stream=None) -> None:

@@ -247,6 +247,76 @@ extern "C" int zero_adam_shard(const zero_plan_t* plan, int32_t group, float* ma
                                      d_coef, mode, out, (cudaStream_t)stream));
 }
 
+// Norm partials the clipped step writes: one zero_rs_partials() count per
+// reduce-scatter window of `bucket` elements.
+static int64_t clipped_partials(const zero_plan_t* plan, int32_t group, int gdtype,
+                                int64_t bucket) {
+  const int64_t P = plan->groups[group].psi_pad;
+  int64_t n = 0;
+  for (int64_t a = 0; a < P; a += bucket)
+    n += zk::rs_partials_for(plan->n_ranks, gdtype, (P - a < bucket ? P - a : bucket));
+  return n;
+}
+
+extern "C" int zero_step_clipped_partials(const zero_plan_t* plan, int32_t group,
+                                          zero_dtype_t gdtype, int64_t bucket,
+                                          int64_t* n_partials) {
+  ZERO_TRY(check_group(plan, group));
+  if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
+  if (bucket < 1 || !n_partials) return ZERO_EINVAL;
+  *n_partials = clipped_partials(plan, group, gdtype, bucket);
+  return ZERO_OK;
+}
+
+extern "C" int zero_step_clipped(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                                 zero_dtype_t gdtype, float* reduced, float* master, float* m,
+                                 float* v, const zero_adam_t* hp, float max_norm, int64_t bucket,
+                                 int64_t chunk, double* partials, int64_t n_partials,
+                                 float* d_norm, float* d_coef, void* full_out,
+                                 zero_dtype_t out_dtype, zero_stream_t stream) {
+  NvtxRange nvtx("zero_step_clipped");
+  ZERO_TRY(check_group(plan, group));
+  if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_rank_ptrs(plan, grads));
+  ZERO_TRY(check_buf(reduced));
+  ZERO_TRY(check_buf(master));
+  ZERO_TRY(check_buf(m));
+  ZERO_TRY(check_buf(v));
+  ZERO_TRY(check_opt_buf(full_out));
+  if (full_out && !dtype_ok(out_dtype)) return ZERO_EDTYPE;
+  if (!partials || !d_coef || bucket < 1 || chunk < 1) return ZERO_EINVAL;
+  if (!isfinite(max_norm) || max_norm <= 0.0f) return ZERO_EINVAL;
+  ZERO_TRY(check_opt_f64(partials));
+  ZERO_TRY(check_opt_f32(d_norm));
+  ZERO_TRY(check_opt_f32(d_coef));
+  zk::AdamK k;
+  ZERO_TRY(adam_k(hp, &k));
+  if (n_partials < clipped_partials(plan, group, gdtype, bucket)) return ZERO_ERANGE;
+  const cudaStream_t st = (cudaStream_t)stream;
+  const zk::RankPtrs src = rank_ptrs(plan, grads);
+  const zk::GroupK g = group_k(plan, group);
+  const int64_t P = plan->groups[group].psi_pad;
+  // 1. reduce-scatter window by window, each writing its slice of partials
+  cudaError_t e = cudaSuccess;
+  int64_t off = 0;
+  for (int64_t a = 0; a < P && e == cudaSuccess; a += bucket) {
+    const int64_t b = P - a < bucket ? P : a + bucket;
+    e = zk::launch_reduce_scatter(src, gdtype, g, reduced, a, b, hp->grad_scale, partials + off,
+                                  zk::RS_STORE, st);
+    off += zk::rs_partials_for(plan->n_ranks, gdtype, b - a);
+  }
+  // 2. global norm and clip coefficient on the device
+  if (e == cudaSuccess) e = zk::launch_norm(partials, off, max_norm, d_norm, d_coef, st);
+  // 3. Adam chunk by chunk with the coefficient, writing the gathered output
+  const int mode = !full_out ? zk::OUT_NONE
+                             : (out_dtype == ZERO_BF16 ? zk::OUT_FULL_BF16 : zk::OUT_FULL_F32);
+  for (int64_t a = 0; a < P && e == cudaSuccess; a += chunk) {
+    const int64_t b = P - a < chunk ? P : a + chunk;
+    e = zk::launch_adam(g, a, b, master, m, v, reduced, k, d_coef, mode, full_out, st);
+  }
+  return cuda_status(e);
+}
+
 extern "C" int zero_all_gather(const zero_plan_t* plan, int32_t group, const float* master,
                                void* full_out, zero_dtype_t out_dtype, zero_stream_t stream) {
   NvtxRange nvtx("zero_all_gather");
