@@ -31,6 +31,25 @@ def test_reference_arm_prints_the_contract_line():
     assert d["config"] == bench.fused_config(W.GPT2_SMALL, 1)
 
 
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as the driver launches N > 1 (torchrun, 2 ranks, gloo on the
+    CPU): rank 0 alone runs the oracle and prints the line; rank 1 exits 0."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                          "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                          "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                          "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [x for x in out.stdout.splitlines() if x.strip().startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
 def test_clock_sampler_parses_rows_and_reasons():
     cs = bench.ClockSampler(0)
     cs.out = "\n".join([
