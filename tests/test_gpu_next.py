@@ -152,6 +152,41 @@ def test_occupancy_setting_does_not_change_results(cuda):
         assert abs(r[5] - base[5]) <= 1e-6 * base[5]
 
 
+def test_gather_occupancy_settings_do_not_change_results(cuda):
+    """The bulk gather's CTAs per SM (ZERO_OCC_GATHER, ZERO_OCC_PREFETCH)
+    and the consumer's blocks (ZERO_OCC_CONSUMER) change only which CTA moves
+    which piece: gathered layers and the pass's checksums are identical for
+    every setting, including caps the shared memory cannot hold at once."""
+    import torch
+    d, ffn, vocab = 64, 172, 500
+    blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(3)]
+    numels = [vocab * d] + [n for b in blocks for n in b] + [d, vocab * d]
+    groups = [0] + [1 + i // 9 for i in range(27)] + [4, 4]
+    c = Case(numels, 16, 16, "bf16", seed=8, groups=groups, host_state=False)
+    Z = c.Z
+    N, G = 16, len(c.groups)
+    shards = [torch.randn(c.info["shard_total"], device=cuda).to(torch.bfloat16) for _ in range(N)]
+    gmax = max(g["psi_pad"] for g in c.groups)
+    order = list(range(G)) + list(reversed(range(G)))
+    results = []
+    for cap in (1, 3, 12, 0):
+        for kind in (Z.ZERO_OCC_GATHER, Z.ZERO_OCC_PREFETCH, Z.ZERO_OCC_CONSUMER):
+            Z.zero_set_occupancy(kind, cap)
+        layers = [torch.empty(g["psi_pad"], dtype=torch.bfloat16, device=cuda) for g in c.groups]
+        for gi in range(G):
+            Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, layers[gi])
+        bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=cuda) for _ in range(2)]
+        sums = torch.zeros(len(order), dtype=torch.int64, device=cuda)
+        Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums, 9,
+                                  torch.cuda.current_stream(), torch.cuda.Stream())
+        torch.cuda.synchronize()
+        results.append((layers, sums))
+    base = results[-1]
+    for layers, sums in results[:-1]:
+        assert all(torch.equal(x, y) for x, y in zip(layers, base[0]))
+        assert torch.equal(sums, base[1])
+
+
 def test_stage3_per_parameter_partitioning(cuda):
     """Per-parameter partitioning (each tensor its own group, sharded over
     the N ranks and padded on its own): step and gather of every tensor
