@@ -145,6 +145,70 @@ def test_planner_from_several_host_threads():
     assert not errors, errors[0]
 
 
+def test_random_calls_return_a_status_and_never_crash():
+    """2 000 seeded random calls of the device entry points with random
+    groups, windows, sizes, dtypes and (never dereferenced) addresses: each
+    returns a known status code.  Host-only: with no GPU present any call
+    that passes its checks fails at the launch with ZERO_ECUDA; it is skipped
+    where a GPU is present, since there it could launch on bogus addresses."""
+    import numpy as np
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch kernels on fake addresses")
+    lib = Z.binding._lib()
+    codes = {Z.ZERO_OK, Z.ZERO_EINVAL, Z.ZERO_EALIGN, Z.ZERO_ERANGE, Z.ZERO_EDTYPE,
+             Z.ZERO_ENOMEM, Z.ZERO_ECUDA, Z.ZERO_ETIMEOUT}
+    rng = np.random.default_rng(99)
+    plans = [Z.zero_plan([int(x) for x in rng.integers(0, 5000, int(rng.integers(1, 8)))],
+                         int(rng.integers(1, 17)), int(rng.choice([1, 8, 16])),
+                         None) for _ in range(6)]
+    addrs = [0, 1 << 40, (1 << 40) + 16, (1 << 40) + 4, (1 << 40) + 8]
+
+    def addr():
+        return int(rng.choice(addrs))
+
+    def ptrs(n):
+        return [addr() for _ in range(max(0, n))]
+
+    hp = Z.adam_hp(int(rng.integers(0, 3)), 0.25)
+    seen = set()
+    for _ in range(2000):
+        p = plans[int(rng.integers(0, len(plans)))]
+        n = Z.zero_plan_info(p)["n_ranks"]
+        g = int(rng.integers(-1, 3))
+        a, b = (int(x) for x in rng.integers(-5, 12000, 2))
+        dt = int(rng.integers(-1, 3))
+        which = int(rng.integers(0, 8))
+        B = Z.binding
+        if which == 0:
+            st = lib.zero_reduce_scatter(p, g, B._ptr_array(ptrs(n)), dt, addr(), a, b, 0.5,
+                                         addr(), None)
+        elif which == 1:
+            st = lib.zero_step(p, g, B._ptr_array(ptrs(n)), dt, addr(), addr(), addr(),
+                               B.ctypes.byref(hp), addr(), addr(), dt, None)
+        elif which == 2:
+            st = lib.zero_adam_shard(p, g, addr(), addr(), addr(), addr(), B.ctypes.byref(hp),
+                                     addr(), a, b, addr(), dt, None)
+        elif which == 3:
+            st = lib.zero_all_gather(p, g, addr(), addr(), dt, None)
+        elif which == 4:
+            st = lib.zero_gather_layer(p, g, B._ptr_array(ptrs(n)), dt, addr(), None)
+        elif which == 5:
+            k = int(rng.integers(0, 4))
+            grp = (B.c_i32 * max(1, k))(*[int(x) for x in rng.integers(-1, 3, k)])
+            st = lib.zero_gather_groups(p, grp, k, B._ptr_array(ptrs(n)), dt,
+                                        B._ptr_array(ptrs(k)), None)
+        elif which == 6:
+            st = lib.zero_grad_norm(addr(), a, float(rng.choice([1.0, 0.0, -1.0])), addr(),
+                                    addr(), None)
+        else:
+            st = lib.zero_copy(addr(), addr(), a, None)
+        assert st in codes, (which, st)
+        seen.add(st)
+    # the random arguments reach every kind of check and, past them, the launch
+    assert {Z.ZERO_EINVAL, Z.ZERO_EALIGN, Z.ZERO_ERANGE, Z.ZERO_EDTYPE} <= seen, seen
+
+
 def test_plan_argument_errors():
     for args in [([4], 0, 1), ([4], 65, 1), ([4], 2, 0), ([-1], 2, 1)]:
         with pytest.raises(Z.ZeroError) as e:
