@@ -690,6 +690,28 @@ def bench_gather_sweep(w, steps: int, dist: Dist, only=None) -> dict:
         res[per] = {"groups": len(groups), "gathers": len(order), "ms": ms,
                     "gbs": 4 * elems / (ms * 1e-3) / 1e9,
                     "mean_gather_mb": 2 * elems / len(order) / 1e6}
+        if per in ("tensor-coalesced", "layer"):
+            # the two-stream pass (prefetch on stream B, one-round consumer on A)
+            sums = torch.zeros(len(order), dtype=torch.int64, device=dev)
+            sb = torch.cuda.Stream(dev)
+            if per == "layer":
+                run = lambda: Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums,
+                                                        1, sa, sb)
+            else:
+                step_groups = [spans[L][0] for L in order]
+                run = lambda: Z.zero_stage3_gather_pass_steps(plan, step_groups, shards, bufs,
+                                                              gmax, sums, 1, sa, sb)
+            run()
+            torch.cuda.synchronize()
+            pass_ms = []
+            for _ in range(steps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(sa)
+                run()
+                e1.record(sa)
+                torch.cuda.synchronize()
+                pass_ms.append(e0.elapsed_time(e1))
+            res[per]["pass_ms"] = statistics.fmean(pass_ms)
         del shards, bufs
         torch.cuda.empty_cache()
     return res

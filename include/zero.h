@@ -347,6 +347,23 @@ int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* order, int32
                             int64_t buf_elems, uint64_t* d_sums, int32_t consumer_rounds,
                             zero_stream_t stream_a, zero_stream_t stream_b);
 
+/* zero_stage3_gather_pass_steps: zero_stage3_gather_pass whose step j
+ * fetches several groups at once, step_groups[step_first[j]] ..
+ * step_groups[step_first[j+1] - 1] (1 to ZERO_MAX_COALESCE groups;
+ * step_first[0] = 0, n_steps + 1 entries), as zero_gather_groups does: into
+ * layer_bufs[j % 2] one after another, each at the running element offset,
+ * and the consumer then reads the step's sum of psi_pad elements as one
+ * layer.  Made for per-parameter partitioning, where a module's tensors are
+ * separate groups fetched together.  In a step of more than one group every
+ * group's psi_pad * 2 bytes must be a multiple of 16 (ZERO_EALIGN otherwise),
+ * and each step's elements must fit buf_elems (ZERO_ERANGE).  Otherwise as
+ * zero_stage3_gather_pass. */
+int zero_stage3_gather_pass_steps(const zero_plan_t* plan, const int32_t* step_first,
+                                  const int32_t* step_groups, int32_t n_steps,
+                                  const void* const* shards, void* const* layer_bufs,
+                                  int64_t buf_elems, uint64_t* d_sums, int32_t consumer_rounds,
+                                  zero_stream_t stream_a, zero_stream_t stream_b);
+
 /* zero_layer_checksum: stands in for the layer computation that consumes a
  * gathered buffer of n bf16 bit patterns (no counterpart on the pages).  For
  * each 8-element vector v (and each element of a ragged tail on its own),

@@ -261,6 +261,57 @@ def test_native_gather_schedule_matches_direct_gathers(cuda):
         assert e.value.status == status
 
 
+def test_gather_pass_with_coalesced_steps(cuda):
+    """Per-parameter partitioning with the two-stream pass: each step fetches
+    one module's tensor groups together (zero_stage3_gather_pass_steps); the
+    consumer's checksum of every step equals the oracle's over the
+    concatenated gathered tensors, forward and reverse."""
+    import torch
+    d, ffn, vocab = 64, 172, 500
+    blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(3)]
+    numels = [vocab * d] + [n for b in blocks for n in b] + [d, vocab * d]
+    layer_of = [0] + [1 + i // 9 for i in range(27)] + [4, 4]
+    groups = list(range(len(numels)))                      # every tensor its own group
+    c = Case(numels, 16, 16, "bf16", seed=13, groups=groups, host_state=False)
+    Z = c.Z
+    N = 16
+    rng = np.random.default_rng(13)
+    host = [rng.integers(0, 1 << 16, c.info["shard_total"], dtype=np.uint64).astype(np.uint16)
+            for _ in range(N)]
+    shards = [torch.from_numpy(h.view(np.int16)).to(cuda) for h in host]
+    layers = [[t for t, L in enumerate(layer_of) if L == k] for k in range(5)]
+    steps = layers + layers[::-1]
+    elems = [sum(c.groups[g]["psi_pad"] for g in st) for st in steps]
+    bufs = [torch.empty(max(elems), dtype=torch.bfloat16, device=cuda) for _ in range(2)]
+    sums = torch.zeros(len(steps), dtype=torch.int64, device=cuda)
+    Z.zero_stage3_gather_pass_steps(c.plan, steps, shards, bufs, max(elems), sums, 5,
+                                    torch.cuda.current_stream(), torch.cuda.Stream())
+    torch.cuda.synchronize()
+    for j, st in enumerate(steps):
+        parts = []
+        for g in st:
+            gi = c.groups[g]
+            want, _, _ = O.gather_layer([h[gi["rank_off"]:gi["rank_off"] + gi["shard"]]
+                                         for h in host])
+            parts.append(want)
+        assert int(sums[j].item()) % (1 << 64) == O.layer_checksum(np.concatenate(parts), 5), j
+    E = Z.ZeroError
+    with pytest.raises(E) as e:                           # a step must fit the buffers
+        Z.zero_stage3_gather_pass_steps(c.plan, steps, shards, bufs, max(elems) - 1, sums, 1,
+                                        torch.cuda.current_stream(), torch.cuda.Stream())
+    assert e.value.status == Z.ZERO_ERANGE
+    odd = Case([5, 7, 9], 3, 1, "bf16", seed=1, groups=[0, 1, 2], host_state=False)
+    osh = [torch.zeros(odd.info["shard_total"], dtype=torch.bfloat16, device=cuda)
+           for _ in range(3)]
+    with pytest.raises(E) as e:                           # packed outputs must stay aligned
+        Z.zero_stage3_gather_pass_steps(odd.plan, [[0, 1]], osh, bufs, max(elems), sums, 1,
+                                        torch.cuda.current_stream(), torch.cuda.Stream())
+    assert e.value.status == Z.ZERO_EALIGN
+    Z.zero_stage3_gather_pass_steps(odd.plan, [[0], [1], [2]], osh, bufs, max(elems), sums, 1,
+                                    torch.cuda.current_stream(), torch.cuda.Stream())
+    torch.cuda.synchronize()
+
+
 def test_cuda_graph_of_the_stage3_gather_pass(cuda):
     """The two-stream gather schedule captured once in a CUDA graph (stream B
     forks from and joins the capturing stream through the pass's events);

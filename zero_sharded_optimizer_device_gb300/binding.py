@@ -133,6 +133,8 @@ _SIGS = {
     "zero_layer_checksum": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp]),
     "zero_stage3_gather_pass": (c_i32, [c_vp, P(c_i32), c_i32, P(c_vp), P(c_vp), c_i64, c_vp,
                                         c_i32, c_vp, c_vp]),
+    "zero_stage3_gather_pass_steps": (c_i32, [c_vp, P(c_i32), P(c_i32), c_i32, P(c_vp),
+                                              P(c_vp), c_i64, c_vp, c_i32, c_vp, c_vp]),
     "zero_copy": (c_i32, [c_vp, c_vp, c_i64, c_vp]),
     "zero_adam_state_init": (c_i32, [P(zero_adam_t), c_vp, c_vp]),
     "zero_adam_state_advance": (c_i32, [P(zero_adam_t), c_vp, c_vp]),
@@ -436,6 +438,23 @@ def zero_stage3_gather_pass(plan, order, shards, layer_bufs, buf_elems, d_sums,
                                           _ptr_array(layer_bufs), buf_elems, _ptr(d_sums),
                                           consumer_rounds, _stream(stream_a), _stream(stream_b)),
            "zero_stage3_gather_pass")
+
+
+def zero_stage3_gather_pass_steps(plan, steps, shards, layer_bufs, buf_elems, d_sums,
+                                  consumer_rounds, stream_a, stream_b) -> None:
+    """steps: a list of group lists, one per step (the C call's step_first
+    and step_groups are built from it)."""
+    first = [0]
+    for st in steps:
+        first.append(first[-1] + len(st))
+    flat = [int(g) for st in steps for g in st]
+    fa = (c_i32 * len(first))(*first)
+    ga = (c_i32 * max(1, len(flat)))(*flat)
+    _check(_lib().zero_stage3_gather_pass_steps(plan, fa, ga, len(steps), _ptr_array(shards),
+                                                _ptr_array(layer_bufs), buf_elems, _ptr(d_sums),
+                                                consumer_rounds, _stream(stream_a),
+                                                _stream(stream_b)),
+           "zero_stage3_gather_pass_steps")
 
 
 def zero_layer_checksum(layer, n, rounds, d_out, stream=None) -> None:
