@@ -620,6 +620,36 @@ def test_stage3_unaligned_shards(cuda):
                     f"group {gi}")
 
 
+@pytest.mark.parametrize("sigma", [1e-21, 1e-30, 3e18, 1e21])
+def test_subnormal_and_overflowing_moments_match_the_oracle(cuda, sigma):
+    """Gradient scales whose squares are subnormal (1e-21), underflow to zero
+    (1e-30), stay large but finite (3e18) or overflow fp32 (1e21) take
+    the same IEEE path on the GPU as in the oracle: no flush to zero, the
+    same infinities, bit for bit over three steps."""
+    import torch
+    c = Case([5000, 123], 8, 16, "f32", grad_sigma=sigma, seed=23)
+    Z = c.Z
+    out = torch.empty(c.info["psi_pad"], dtype=torch.float32, device=cuda)
+    r = None
+    for s in range(1, 4):
+        Z.zero_step(c.plan, 0, c.grads_dev(0, s), Z.ZERO_F32, c.master, c.m, c.v, c.hp_dev(s),
+                    None, out, Z.ZERO_F32)
+        with np.errstate(over="ignore", invalid="ignore"):
+            r = c.oracle_step(0, s, out_dtype="f32")
+    torch.cuda.synchronize()
+    v = c.v.cpu().numpy()
+    if sigma == 1e-21:
+        assert ((v > 0) & (v < np.finfo(np.float32).tiny)).any()   # subnormals reached
+    if sigma == 1e-30:
+        assert (v == 0).all()                                    # g*g underflows to zero
+    if sigma > 1e20:
+        assert np.isinf(v).any()
+    c.check_state(f"sigma {sigma}")
+    got = out.cpu().numpy()
+    same = (got.view(np.uint32) == r["full"].view(np.uint32)) | (np.isnan(got) & np.isnan(r["full"]))
+    assert same.all()
+
+
 def test_non_finite_gradients_propagate_like_the_oracle(cuda):
     """A NaN or an infinity in one rank's gradient poisons exactly the
     elements it touches, on both sides; every other element stays
