@@ -681,6 +681,45 @@ def test_non_finite_gradients_propagate_like_the_oracle(cuda):
     assert np.isnan(O.bf16_to_f32(ob[nan_w])).all()
 
 
+def test_bf16_cast_of_special_values_on_the_gpu(cuda):
+    """The GPU's fp32 -> bf16 casts (all-gather, and the fused step with zero
+    gradients, which leaves the master unchanged) agree bit for bit with the
+    oracle's round-to-nearest-even on ties, carries into the exponent,
+    signed zeros, subnormals, infinities, the largest finite values and
+    NaNs."""
+    import torch
+    rng = np.random.default_rng(5)
+    hi = rng.integers(0, 1 << 16, 4096, dtype=np.uint64).astype(np.uint32) << 16
+    special = np.array([0x00000000, 0x80000000, 0x00000001, 0x807FFFFF, 0x7F7FFFFF, 0xFF7FFFFF,
+                        0x7F7F8000, 0x3F808000, 0x3F818000, 0x3FFF8000, 0x7F800000, 0xFF800000,
+                        0x7FC00000, 0x7F800001, 0xFFC12345, 0x3F800001, 0x3F807FFF],
+                       dtype=np.uint32)
+    bits = np.concatenate([hi | 0x8000, hi | 0x7FFF, hi | 0x8001, special])   # ties, below, above
+    c = Case([bits.size], 4, 16, "f32", seed=3, host_state=False)
+    Z = c.Z
+    P = c.info["psi_pad"]
+    host = np.zeros(P, np.uint32)
+    host[:bits.size] = bits
+    c.master.copy_(torch.from_numpy(host.view(np.int32)).to(cuda).view(torch.float32))
+    out = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    Z.zero_all_gather(c.plan, 0, c.master, out, Z.ZERO_BF16)
+    torch.cuda.synchronize()
+    want = O.f32_to_bf16(host.view(np.float32))
+    got = bits_of(out)
+    nan = np.isnan(host.view(np.float32))
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.isnan(O.bf16_to_f32(got[nan])).all()
+    zeros = [torch.zeros(P, dtype=torch.float32, device=cuda) for _ in range(4)]
+    out2 = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    Z.zero_step(c.plan, 0, zeros, Z.ZERO_F32, c.master, c.m, c.v, c.hp_dev(1), None, out2,
+                Z.ZERO_BF16)
+    torch.cuda.synchronize()
+    mb = bits_of(c.master)                                  # zero gradients: master unchanged
+    assert np.array_equal(mb[~nan], host[~nan]) and np.isnan(mb.view(np.float32)[nan]).all()
+    got2 = bits_of(out2)
+    assert np.array_equal(got2[~nan], want[~nan]) and np.isnan(O.bf16_to_f32(got2[nan])).all()
+
+
 def test_zero_gradients_leave_parameters_unchanged(cuda):
     import torch
     c = Case([3000, 17], 8, 16, "bf16", seed=19, host_state=False)
