@@ -650,19 +650,20 @@ def test_subnormal_and_overflowing_moments_match_the_oracle(cuda, sigma):
     assert same.all()
 
 
-def test_non_finite_gradients_propagate_like_the_oracle(cuda):
-    """A NaN or an infinity in one rank's gradient poisons exactly the
-    elements it touches, on both sides; every other element stays
+@pytest.mark.parametrize("gd", ["f32", "bf16"])
+def test_non_finite_gradients_propagate_like_the_oracle(cuda, gd):
+    """A NaN or an infinity in one rank's gradient (fp32 or bf16) poisons
+    exactly the elements it touches, on both sides; every other element stays
     bit-identical to the oracle."""
     import torch
-    c = Case([4096], 4, 16, "f32", grad_sigma=1e-2, seed=17)
+    c = Case([4096], 4, 16, gd, grad_sigma=1e-2, seed=17)
     Z = c.Z
     grads = c.grads_dev(0, 1)
     bad = {10: float("nan"), 777: float("inf"), 2048: float("-inf")}
     for i, x in bad.items():
         grads[i % 4][i] = x
     out = torch.empty(c.info["psi_pad"], dtype=torch.bfloat16, device=cuda)
-    Z.zero_step(c.plan, 0, grads, Z.ZERO_F32, c.master, c.m, c.v, c.hp_dev(1), None, out,
+    Z.zero_step(c.plan, 0, grads, c.zdtype, c.master, c.m, c.v, c.hp_dev(1), None, out,
                 Z.ZERO_BF16)
     local = c.grads_host(0, 1)
     for i, x in bad.items():
