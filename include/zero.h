@@ -243,9 +243,10 @@ int zero_adam_shard(const zero_plan_t* plan, int32_t group, float* master, float
                     int64_t begin, int64_t end, void* out, zero_dtype_t out_dtype,
                     zero_stream_t stream);
 
-/* zero_step_clipped: the step with gradient clipping of group g in one call
- * (the path of a run that clips: the reduced gradient has to exist before
- * its global norm does).  The plain step zero_step cannot clip by the norm
+/* zero_step_clipped [P1 "Problem"; P3; KB; the clip is not on the pages]:
+ * the step with gradient clipping of group g in one call (the path of a run
+ * that clips: the reduced gradient has to exist before its global norm
+ * does).  The plain step zero_step cannot clip by the norm
  * of the step's own gradient, since it never materialises the reduced
  * gradient; this call strings the unfused calls together on `stream`, with
  * results identical, bit for bit, to making them one by one:
