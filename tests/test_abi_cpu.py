@@ -209,6 +209,21 @@ def test_random_calls_return_a_status_and_never_crash():
     assert {Z.ZERO_EINVAL, Z.ZERO_EALIGN, Z.ZERO_ERANGE, Z.ZERO_EDTYPE} <= seen, seen
 
 
+def test_binding_refuses_pointer_lists_of_the_wrong_length():
+    """The C side reads exactly N per-rank addresses (and one output per
+    group, two layer buffers): a list of another length never reaches it."""
+    p = Z.zero_plan([1000], 4, 16)
+    A = 1 << 40
+    with pytest.raises(ValueError):
+        Z.zero_reduce_scatter(p, 0, [A, A, A], Z.ZERO_BF16, A, 0, 16, 0.25, None, 0)
+    with pytest.raises(ValueError):
+        Z.zero_gather_layer(p, 0, [A] * 5, Z.ZERO_BF16, A, 0)
+    with pytest.raises(ValueError):
+        Z.zero_gather_groups(p, [0, 0], [A] * 4, Z.ZERO_BF16, [A], 0)
+    with pytest.raises(ValueError):
+        Z.zero_stage3_gather_pass(p, [0], [A] * 4, [A], 16, A, 1, 1, 2)
+
+
 def test_plan_argument_errors():
     for args in [([4], 0, 1), ([4], 65, 1), ([4], 2, 0), ([-1], 2, 1)]:
         with pytest.raises(Z.ZeroError) as e:

@@ -245,11 +245,20 @@ def _stream(s) -> int | None:
     return s.cuda_stream
 
 
-def _ptr_array(xs):
-    arr = (c_vp * len(xs))()
+def _ptr_array(xs, n: int | None = None, what: str = "buffers"):
+    """A host array of addresses; with n, the C side reads exactly n of them,
+    so a list of another length is refused here."""
+    if n is not None and len(xs) != n:
+        raise ValueError(f"{what}: {len(xs)} given, the call reads {n}")
+    arr = (c_vp * max(1, len(xs)))()
     for i, x in enumerate(xs):
         arr[i] = _ptr(x)
     return arr
+
+
+def _ranks(plan, xs, what: str = "per-rank buffers"):
+    """The plan's N per-rank buffers (gradients or shards) as a host array."""
+    return _ptr_array(xs, plan.n_ranks, what)
 
 
 def _check(status: int, func: str) -> None:
@@ -260,8 +269,9 @@ def _check(status: int, func: str) -> None:
 class Plan:
     """Owns a zero_plan_t*; destroyed with the object."""
 
-    def __init__(self, handle: int):
+    def __init__(self, handle: int, n_ranks: int = 0):
         self.handle = handle
+        self.n_ranks = n_ranks
 
     def __del__(self):
         h, self.handle = getattr(self, "handle", None), None
@@ -294,7 +304,7 @@ def zero_plan(numels, n_ranks: int, align: int = 16, group_of_tensor=None) -> Pl
         groups = (c_i32 * max(n, 1))(*[int(g) for g in group_of_tensor])
     out = c_vp()
     _check(_lib().zero_plan(arr, n, n_ranks, align, groups, ctypes.byref(out)), "zero_plan")
-    return Plan(out.value)
+    return Plan(out.value, n_ranks)
 
 
 def zero_plan_destroy(plan: Plan) -> None:
@@ -359,14 +369,16 @@ def zero_rs_partials(plan: Plan, gdtype: int, n_elements: int) -> int:
 
 def zero_reduce_scatter(plan, group, grads, gdtype, reduced, begin, end, grad_scale,
                         sumsq_partials=None, stream=None) -> None:
-    _check(_lib().zero_reduce_scatter(plan, group, _ptr_array(grads), gdtype, _ptr(reduced),
+    grad_ptrs = _ranks(plan, grads, "grads")
+    _check(_lib().zero_reduce_scatter(plan, group, grad_ptrs, gdtype, _ptr(reduced),
                                       begin, end, grad_scale, _ptr(sumsq_partials),
                                       _stream(stream)), "zero_reduce_scatter")
 
 
 def zero_reduce_scatter_acc(plan, group, grads, gdtype, reduced, begin, end, grad_scale,
                             sumsq_partials=None, stream=None) -> None:
-    _check(_lib().zero_reduce_scatter_acc(plan, group, _ptr_array(grads), gdtype, _ptr(reduced),
+    grad_ptrs = _ranks(plan, grads, "grads")
+    _check(_lib().zero_reduce_scatter_acc(plan, group, grad_ptrs, gdtype, _ptr(reduced),
                                           begin, end, grad_scale, _ptr(sumsq_partials),
                                           _stream(stream)), "zero_reduce_scatter_acc")
 
@@ -393,7 +405,8 @@ def zero_step_clipped_partials(plan, group, gdtype, bucket) -> int:
 def zero_step_clipped(plan, group, grads, gdtype, reduced, master, m, v, hp, max_norm, bucket,
                       chunk, partials, n_partials, d_norm, d_coef, full_out,
                       out_dtype=ZERO_BF16, stream=None) -> None:
-    _check(_lib().zero_step_clipped(plan, group, _ptr_array(grads), gdtype, _ptr(reduced),
+    grad_ptrs = _ranks(plan, grads, "grads")
+    _check(_lib().zero_step_clipped(plan, group, grad_ptrs, gdtype, _ptr(reduced),
                                     _ptr(master), _ptr(m), _ptr(v), ctypes.byref(hp), max_norm,
                                     bucket, chunk, _ptr(partials), n_partials, _ptr(d_norm),
                                     _ptr(d_coef), _ptr(full_out), out_dtype, _stream(stream)),
@@ -407,35 +420,43 @@ def zero_all_gather(plan, group, master, full_out, out_dtype=ZERO_BF16, stream=N
 
 def zero_step(plan, group, grads, gdtype, master, m, v, hp, d_coef, full_out,
               out_dtype=ZERO_BF16, stream=None) -> None:
-    _check(_lib().zero_step(plan, group, _ptr_array(grads), gdtype, _ptr(master), _ptr(m),
+    grad_ptrs = _ranks(plan, grads, "grads")
+    _check(_lib().zero_step(plan, group, grad_ptrs, gdtype, _ptr(master), _ptr(m),
                             _ptr(v), ctypes.byref(hp), _ptr(d_coef), _ptr(full_out), out_dtype,
                             _stream(stream)), "zero_step")
 
 
 def zero_step_group(plan, group, grads, gdtype, master, m, v, hp, d_coef, shards,
                     stream=None) -> None:
-    _check(_lib().zero_step_group(plan, group, _ptr_array(grads), gdtype, _ptr(master), _ptr(m),
-                                  _ptr(v), ctypes.byref(hp), _ptr(d_coef), _ptr_array(shards),
+    grad_ptrs = _ranks(plan, grads, "grads")
+    shard_ptrs = _ranks(plan, shards, "shards")
+    _check(_lib().zero_step_group(plan, group, grad_ptrs, gdtype, _ptr(master), _ptr(m),
+                                  _ptr(v), ctypes.byref(hp), _ptr(d_coef), shard_ptrs,
                                   _stream(stream)), "zero_step_group")
 
 
 def zero_gather_layer(plan, group, shards, dtype, layer_out, stream=None) -> None:
-    _check(_lib().zero_gather_layer(plan, group, _ptr_array(shards), dtype, _ptr(layer_out),
+    shard_ptrs = _ranks(plan, shards, "shards")
+    _check(_lib().zero_gather_layer(plan, group, shard_ptrs, dtype, _ptr(layer_out),
                                     _stream(stream)), "zero_gather_layer")
 
 
 def zero_gather_groups(plan, groups, shards, dtype, layer_outs, stream=None) -> None:
+    shard_ptrs = _ranks(plan, shards, "shards")
+    out_ptrs = _ptr_array(layer_outs, len(groups), "layer_outs")
     arr = (c_i32 * max(1, len(groups)))(*[int(g) for g in groups])
-    _check(_lib().zero_gather_groups(plan, arr, len(groups), _ptr_array(shards), dtype,
-                                     _ptr_array(layer_outs), _stream(stream)),
+    _check(_lib().zero_gather_groups(plan, arr, len(groups), shard_ptrs, dtype,
+                                     out_ptrs, _stream(stream)),
            "zero_gather_groups")
 
 
 def zero_stage3_gather_pass(plan, order, shards, layer_bufs, buf_elems, d_sums,
                             consumer_rounds, stream_a, stream_b) -> None:
+    shard_ptrs = _ranks(plan, shards, "shards")
+    buf_ptrs = _ptr_array(layer_bufs, 2, "layer_bufs")
     arr = (c_i32 * max(1, len(order)))(*[int(g) for g in order])
-    _check(_lib().zero_stage3_gather_pass(plan, arr, len(order), _ptr_array(shards),
-                                          _ptr_array(layer_bufs), buf_elems, _ptr(d_sums),
+    _check(_lib().zero_stage3_gather_pass(plan, arr, len(order), shard_ptrs,
+                                          buf_ptrs, buf_elems, _ptr(d_sums),
                                           consumer_rounds, _stream(stream_a), _stream(stream_b)),
            "zero_stage3_gather_pass")
 
@@ -444,14 +465,16 @@ def zero_stage3_gather_pass_steps(plan, steps, shards, layer_bufs, buf_elems, d_
                                   consumer_rounds, stream_a, stream_b) -> None:
     """steps: a list of group lists, one per step (the C call's step_first
     and step_groups are built from it)."""
+    shard_ptrs = _ranks(plan, shards, "shards")
+    buf_ptrs = _ptr_array(layer_bufs, 2, "layer_bufs")
     first = [0]
     for st in steps:
         first.append(first[-1] + len(st))
     flat = [int(g) for st in steps for g in st]
     fa = (c_i32 * len(first))(*first)
     ga = (c_i32 * max(1, len(flat)))(*flat)
-    _check(_lib().zero_stage3_gather_pass_steps(plan, fa, ga, len(steps), _ptr_array(shards),
-                                                _ptr_array(layer_bufs), buf_elems, _ptr(d_sums),
+    _check(_lib().zero_stage3_gather_pass_steps(plan, fa, ga, len(steps), shard_ptrs,
+                                                buf_ptrs, buf_elems, _ptr(d_sums),
                                                 consumer_rounds, _stream(stream_a),
                                                 _stream(stream_b)),
            "zero_stage3_gather_pass_steps")
@@ -495,8 +518,9 @@ def zero_reduce_scatter_norm_static(plan, group, grads, gdtype, reduced, begin, 
     """zero_reduce_scatter + zero_grad_norm for one window with the fp64
     partials in the library's static device array: for callers that cannot
     allocate device memory where they clip (see include/zero.h)."""
+    grad_ptrs = _ranks(plan, grads, "grads")
     _check(_lib().zero_reduce_scatter_norm_static(
-        plan, group, _ptr_array(grads), gdtype, _ptr(reduced), begin, end, grad_scale, max_norm,
+        plan, group, grad_ptrs, gdtype, _ptr(reduced), begin, end, grad_scale, max_norm,
         _ptr(d_norm), _ptr(d_coef), _stream(stream)), "zero_reduce_scatter_norm_static")
 
 
