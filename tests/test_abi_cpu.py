@@ -224,6 +224,29 @@ def test_binding_refuses_pointer_lists_of_the_wrong_length():
         Z.zero_stage3_gather_pass(p, [0], [A] * 4, [A], 16, A, 1, 1, 2)
 
 
+def test_binding_refuses_tensors_too_small_or_strided():
+    """A tensor argument smaller than what the call touches, or not
+    contiguous, is refused before the call (a kernel would run past it)."""
+    import torch
+    p = Z.zero_plan([1000, 24], 4, 16)           # psi_pad 1024
+    ok = torch.zeros(1024)
+    small = torch.zeros(1000)
+    strided = torch.zeros(2048)[::2]
+    g = [torch.zeros(1024, dtype=torch.bfloat16) for _ in range(4)]
+    hp = Z.adam_hp(1, 0.25)
+    with pytest.raises(ValueError, match="master: holds 4000 bytes"):
+        Z.zero_step(p, 0, g, Z.ZERO_BF16, small, ok, ok, hp, None, None, Z.ZERO_BF16, 0)
+    with pytest.raises(ValueError, match="m: not contiguous"):
+        Z.zero_step(p, 0, g, Z.ZERO_BF16, ok, strided, ok, hp, None, None, Z.ZERO_BF16, 0)
+    with pytest.raises(ValueError, match=r"grads\[2\]: holds"):
+        Z.zero_step(p, 0, g[:2] + [torch.zeros(10, dtype=torch.bfloat16), g[3]], Z.ZERO_BF16,
+                    ok, ok, ok, hp, None, None, Z.ZERO_BF16, 0)
+    with pytest.raises(ValueError, match="full_out: holds"):
+        Z.zero_all_gather(p, 0, ok, torch.zeros(100, dtype=torch.bfloat16), Z.ZERO_BF16, 0)
+    with pytest.raises(ValueError, match="reduced: holds"):
+        Z.zero_reduce_scatter(p, 0, g, Z.ZERO_BF16, small, 0, 1024, 0.25, None, 0)
+
+
 def test_plan_argument_errors():
     for args in [([4], 0, 1), ([4], 65, 1), ([4], 2, 0), ([-1], 2, 1)]:
         with pytest.raises(Z.ZeroError) as e:

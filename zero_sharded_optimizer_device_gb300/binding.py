@@ -256,9 +256,38 @@ def _ptr_array(xs, n: int | None = None, what: str = "buffers"):
     return arr
 
 
-def _ranks(plan, xs, what: str = "per-rank buffers"):
-    """The plan's N per-rank buffers (gradients or shards) as a host array."""
+def _ranks(plan, xs, what: str = "per-rank buffers", nbytes: int = 0):
+    """The plan's N per-rank buffers (gradients or shards) as a host array,
+    each tensor checked to hold nbytes."""
+    if len(xs) == plan.n_ranks:
+        for i, x in enumerate(xs):
+            _need(x, nbytes, f"{what}[{i}]")
     return _ptr_array(xs, plan.n_ranks, what)
+
+
+_ESIZE = {ZERO_F32: 4, ZERO_BF16: 2}
+
+
+def _need(x, nbytes: int, what: str):
+    """A tensor argument must be contiguous and hold the nbytes the call
+    touches (a kernel would otherwise run past its end); raw integer
+    addresses are the caller's responsibility, as in the C ABI."""
+    if x is None or isinstance(x, int):
+        return
+    if not x.is_contiguous():
+        raise ValueError(f"{what}: not contiguous")
+    have = x.numel() * x.element_size()
+    if have < nbytes:
+        raise ValueError(f"{what}: holds {have} bytes, the call touches {nbytes}")
+
+
+def _group(plan, group: int):
+    """(flat_off, psi_pad) of a group, or None for an index the library will
+    refuse (it reports the error)."""
+    geo = plan.geometry()
+    if 0 <= group < len(geo["groups"]):
+        return geo["groups"][group]
+    return None
 
 
 def _check(status: int, func: str) -> None:
@@ -272,6 +301,20 @@ class Plan:
     def __init__(self, handle: int, n_ranks: int = 0):
         self.handle = handle
         self.n_ranks = n_ranks
+        self._geometry = None
+
+    def geometry(self) -> dict:
+        """Group offsets and sizes (queried once), for the binding's buffer
+        size checks."""
+        if self._geometry is None:
+            info = zero_plan_info(self)
+            groups = []
+            for g in range(info["n_groups"]):
+                gi = zero_plan_group(self, g)
+                groups.append((gi["flat_off"], gi["psi_pad"]))
+            self._geometry = {"groups": groups, "psi_pad": info["psi_pad"],
+                              "shard_total": info["shard_total"]}
+        return self._geometry
 
     def __del__(self):
         h, self.handle = getattr(self, "handle", None), None
@@ -369,7 +412,12 @@ def zero_rs_partials(plan: Plan, gdtype: int, n_elements: int) -> int:
 
 def zero_reduce_scatter(plan, group, grads, gdtype, reduced, begin, end, grad_scale,
                         sumsq_partials=None, stream=None) -> None:
-    grad_ptrs = _ranks(plan, grads, "grads")
+    g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
+    if g is not None and 0 <= begin <= end <= g[1]:
+        _need(reduced, (g[0] + end) * 4, "reduced")
+        if sumsq_partials is not None and es:
+            _need(sumsq_partials, zero_rs_partials(plan, gdtype, end - begin) * 8, "partials")
+    grad_ptrs = _ranks(plan, grads, "grads", g[1] * es if g else 0)
     _check(_lib().zero_reduce_scatter(plan, group, grad_ptrs, gdtype, _ptr(reduced),
                                       begin, end, grad_scale, _ptr(sumsq_partials),
                                       _stream(stream)), "zero_reduce_scatter")
@@ -377,19 +425,33 @@ def zero_reduce_scatter(plan, group, grads, gdtype, reduced, begin, end, grad_sc
 
 def zero_reduce_scatter_acc(plan, group, grads, gdtype, reduced, begin, end, grad_scale,
                             sumsq_partials=None, stream=None) -> None:
-    grad_ptrs = _ranks(plan, grads, "grads")
+    g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
+    if g is not None and 0 <= begin <= end <= g[1]:
+        _need(reduced, (g[0] + end) * 4, "reduced")
+        if sumsq_partials is not None and es:
+            _need(sumsq_partials, zero_rs_partials(plan, gdtype, end - begin) * 8, "partials")
+    grad_ptrs = _ranks(plan, grads, "grads", g[1] * es if g else 0)
     _check(_lib().zero_reduce_scatter_acc(plan, group, grad_ptrs, gdtype, _ptr(reduced),
                                           begin, end, grad_scale, _ptr(sumsq_partials),
                                           _stream(stream)), "zero_reduce_scatter_acc")
 
 
 def zero_grad_norm(partials, n, max_norm, d_norm, d_coef, stream=None) -> None:
+    _need(partials, max(0, n) * 8, "partials")
+    _need(d_norm, 4, "d_norm")
+    _need(d_coef, 4, "d_coef")
     _check(_lib().zero_grad_norm(_ptr(partials), n, max_norm, _ptr(d_norm), _ptr(d_coef),
                                  _stream(stream)), "zero_grad_norm")
 
 
 def zero_adam_shard(plan, group, master, m, v, reduced, hp, d_coef, begin, end, out,
                     out_dtype=ZERO_BF16, stream=None) -> None:
+    g = _group(plan, group)
+    if g is not None and 0 <= begin <= end <= g[1]:
+        for x, what in ((master, "master"), (m, "m"), (v, "v"), (reduced, "reduced")):
+            _need(x, (g[0] + end) * 4, what)
+        _need(out, (g[0] + end) * _ESIZE.get(out_dtype, 0), "out")
+    _need(d_coef, 4, "d_coef")
     _check(_lib().zero_adam_shard(plan, group, _ptr(master), _ptr(m), _ptr(v), _ptr(reduced),
                                   ctypes.byref(hp), _ptr(d_coef), begin, end, _ptr(out),
                                   out_dtype, _stream(stream)), "zero_adam_shard")
@@ -405,7 +467,15 @@ def zero_step_clipped_partials(plan, group, gdtype, bucket) -> int:
 def zero_step_clipped(plan, group, grads, gdtype, reduced, master, m, v, hp, max_norm, bucket,
                       chunk, partials, n_partials, d_norm, d_coef, full_out,
                       out_dtype=ZERO_BF16, stream=None) -> None:
-    grad_ptrs = _ranks(plan, grads, "grads")
+    g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
+    if g is not None:
+        for x, what in ((reduced, "reduced"), (master, "master"), (m, "m"), (v, "v")):
+            _need(x, (g[0] + g[1]) * 4, what)
+        _need(full_out, (g[0] + g[1]) * _ESIZE.get(out_dtype, 0), "full_out")
+    _need(partials, max(0, n_partials) * 8, "partials")
+    _need(d_norm, 4, "d_norm")
+    _need(d_coef, 4, "d_coef")
+    grad_ptrs = _ranks(plan, grads, "grads", g[1] * es if g else 0)
     _check(_lib().zero_step_clipped(plan, group, grad_ptrs, gdtype, _ptr(reduced),
                                     _ptr(master), _ptr(m), _ptr(v), ctypes.byref(hp), max_norm,
                                     bucket, chunk, _ptr(partials), n_partials, _ptr(d_norm),
@@ -414,13 +484,23 @@ def zero_step_clipped(plan, group, grads, gdtype, reduced, master, m, v, hp, max
 
 
 def zero_all_gather(plan, group, master, full_out, out_dtype=ZERO_BF16, stream=None) -> None:
+    g = _group(plan, group) if group != -1 else (0, plan.geometry()["psi_pad"])
+    if g is not None:
+        _need(master, (g[0] + g[1]) * 4, "master")
+        _need(full_out, (g[0] + g[1]) * _ESIZE.get(out_dtype, 0), "full_out")
     _check(_lib().zero_all_gather(plan, group, _ptr(master), _ptr(full_out), out_dtype,
                                   _stream(stream)), "zero_all_gather")
 
 
 def zero_step(plan, group, grads, gdtype, master, m, v, hp, d_coef, full_out,
               out_dtype=ZERO_BF16, stream=None) -> None:
-    grad_ptrs = _ranks(plan, grads, "grads")
+    g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
+    if g is not None:
+        for x, what in ((master, "master"), (m, "m"), (v, "v")):
+            _need(x, (g[0] + g[1]) * 4, what)
+        _need(full_out, (g[0] + g[1]) * _ESIZE.get(out_dtype, 0), "full_out")
+    _need(d_coef, 4, "d_coef")
+    grad_ptrs = _ranks(plan, grads, "grads", g[1] * es if g else 0)
     _check(_lib().zero_step(plan, group, grad_ptrs, gdtype, _ptr(master), _ptr(m),
                             _ptr(v), ctypes.byref(hp), _ptr(d_coef), _ptr(full_out), out_dtype,
                             _stream(stream)), "zero_step")
@@ -428,21 +508,35 @@ def zero_step(plan, group, grads, gdtype, master, m, v, hp, d_coef, full_out,
 
 def zero_step_group(plan, group, grads, gdtype, master, m, v, hp, d_coef, shards,
                     stream=None) -> None:
-    grad_ptrs = _ranks(plan, grads, "grads")
-    shard_ptrs = _ranks(plan, shards, "shards")
+    g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
+    if g is not None:
+        for x, what in ((master, "master"), (m, "m"), (v, "v")):
+            _need(x, (g[0] + g[1]) * 4, what)
+    _need(d_coef, 4, "d_coef")
+    grad_ptrs = _ranks(plan, grads, "grads", g[1] * es if g else 0)
+    shard_ptrs = _ranks(plan, shards, "shards", plan.geometry()["shard_total"] * 2)
     _check(_lib().zero_step_group(plan, group, grad_ptrs, gdtype, _ptr(master), _ptr(m),
                                   _ptr(v), ctypes.byref(hp), _ptr(d_coef), shard_ptrs,
                                   _stream(stream)), "zero_step_group")
 
 
 def zero_gather_layer(plan, group, shards, dtype, layer_out, stream=None) -> None:
-    shard_ptrs = _ranks(plan, shards, "shards")
+    g, es = _group(plan, group), _ESIZE.get(dtype, 0)
+    if g is not None:
+        _need(layer_out, g[1] * es, "layer_out")
+    shard_ptrs = _ranks(plan, shards, "shards", plan.geometry()["shard_total"] * es)
     _check(_lib().zero_gather_layer(plan, group, shard_ptrs, dtype, _ptr(layer_out),
                                     _stream(stream)), "zero_gather_layer")
 
 
 def zero_gather_groups(plan, groups, shards, dtype, layer_outs, stream=None) -> None:
-    shard_ptrs = _ranks(plan, shards, "shards")
+    es = _ESIZE.get(dtype, 0)
+    if len(layer_outs) == len(groups):
+        for i, (gid, out) in enumerate(zip(groups, layer_outs)):
+            g = _group(plan, int(gid))
+            if g is not None:
+                _need(out, g[1] * es, f"layer_outs[{i}]")
+    shard_ptrs = _ranks(plan, shards, "shards", plan.geometry()["shard_total"] * es)
     out_ptrs = _ptr_array(layer_outs, len(groups), "layer_outs")
     arr = (c_i32 * max(1, len(groups)))(*[int(g) for g in groups])
     _check(_lib().zero_gather_groups(plan, arr, len(groups), shard_ptrs, dtype,
@@ -452,7 +546,11 @@ def zero_gather_groups(plan, groups, shards, dtype, layer_outs, stream=None) -> 
 
 def zero_stage3_gather_pass(plan, order, shards, layer_bufs, buf_elems, d_sums,
                             consumer_rounds, stream_a, stream_b) -> None:
-    shard_ptrs = _ranks(plan, shards, "shards")
+    shard_ptrs = _ranks(plan, shards, "shards", plan.geometry()["shard_total"] * 2)
+    if len(layer_bufs) == 2:
+        for i, b in enumerate(layer_bufs):
+            _need(b, max(0, buf_elems) * 2, f"layer_bufs[{i}]")
+    _need(d_sums, len(order) * 8, "d_sums")
     buf_ptrs = _ptr_array(layer_bufs, 2, "layer_bufs")
     arr = (c_i32 * max(1, len(order)))(*[int(g) for g in order])
     _check(_lib().zero_stage3_gather_pass(plan, arr, len(order), shard_ptrs,
@@ -465,7 +563,11 @@ def zero_stage3_gather_pass_steps(plan, steps, shards, layer_bufs, buf_elems, d_
                                   consumer_rounds, stream_a, stream_b) -> None:
     """steps: a list of group lists, one per step (the C call's step_first
     and step_groups are built from it)."""
-    shard_ptrs = _ranks(plan, shards, "shards")
+    shard_ptrs = _ranks(plan, shards, "shards", plan.geometry()["shard_total"] * 2)
+    if len(layer_bufs) == 2:
+        for i, b in enumerate(layer_bufs):
+            _need(b, max(0, buf_elems) * 2, f"layer_bufs[{i}]")
+    _need(d_sums, len(steps) * 8, "d_sums")
     buf_ptrs = _ptr_array(layer_bufs, 2, "layer_bufs")
     first = [0]
     for st in steps:
@@ -481,16 +583,20 @@ def zero_stage3_gather_pass_steps(plan, steps, shards, layer_bufs, buf_elems, d_
 
 
 def zero_layer_checksum(layer, n, rounds, d_out, stream=None) -> None:
+    _need(layer, max(0, n) * 2, "layer")
+    _need(d_out, 8, "d_out")
     _check(_lib().zero_layer_checksum(_ptr(layer), n, rounds, _ptr(d_out), _stream(stream)),
            "zero_layer_checksum")
 
 
 def zero_adam_state_init(hp, d_state, stream=None) -> None:
+    _need(d_state, ZERO_ADAM_STATE_BYTES, "d_state")
     _check(_lib().zero_adam_state_init(ctypes.byref(hp), _ptr(d_state), _stream(stream)),
            "zero_adam_state_init")
 
 
 def zero_adam_state_advance(hp, d_state, stream=None) -> None:
+    _need(d_state, ZERO_ADAM_STATE_BYTES, "d_state")
     _check(_lib().zero_adam_state_advance(ctypes.byref(hp), _ptr(d_state), _stream(stream)),
            "zero_adam_state_advance")
 
@@ -505,11 +611,15 @@ def zero_set_occupancy(kind: int, blocks_per_sm: int) -> int:
 
 
 def zero_wait_flag(flag, expected, max_polls, d_status, stream=None) -> None:
+    _need(flag, 4, "flag")
+    _need(d_status, 4, "d_status")
     _check(_lib().zero_wait_flag(_ptr(flag), expected, max_polls, _ptr(d_status),
                                  _stream(stream)), "zero_wait_flag")
 
 
 def zero_copy(dst, src, nbytes, stream=None) -> None:
+    _need(dst, max(0, nbytes), "dst")
+    _need(src, max(0, nbytes), "src")
     _check(_lib().zero_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "zero_copy")
 
 
@@ -518,7 +628,12 @@ def zero_reduce_scatter_norm_static(plan, group, grads, gdtype, reduced, begin, 
     """zero_reduce_scatter + zero_grad_norm for one window with the fp64
     partials in the library's static device array: for callers that cannot
     allocate device memory where they clip (see include/zero.h)."""
-    grad_ptrs = _ranks(plan, grads, "grads")
+    g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
+    if g is not None and 0 <= begin <= end <= g[1]:
+        _need(reduced, (g[0] + end) * 4, "reduced")
+    _need(d_norm, 4, "d_norm")
+    _need(d_coef, 4, "d_coef")
+    grad_ptrs = _ranks(plan, grads, "grads", g[1] * es if g else 0)
     _check(_lib().zero_reduce_scatter_norm_static(
         plan, group, grad_ptrs, gdtype, _ptr(reduced), begin, end, grad_scale, max_norm,
         _ptr(d_norm), _ptr(d_coef), _stream(stream)), "zero_reduce_scatter_norm_static")
