@@ -276,7 +276,7 @@ def _need(x, nbytes: int, what: str):
         return
     if not x.is_contiguous():
         raise ValueError(f"{what}: not contiguous")
-    have = x.numel() * x.element_size()
+    have = x.nbytes
     if have < nbytes:
         raise ValueError(f"{what}: holds {have} bytes, the call touches {nbytes}")
 
