@@ -433,6 +433,41 @@ def test_planted_mistakes_fail_a_pin(monkeypatch):
     right = p0.astype(np.float64) - 1e-3 * g.astype(np.float64) / (np.abs(g) + 1e-8)
     assert not np.allclose(wrong, right, atol=4e-9)
 
+    # bf16 by truncation instead of round-to-nearest-even: the torch cast pin
+    x = (rng.standard_normal(4096) * 3).astype(F32)
+    truncated = (x.view(np.uint32) >> 16).astype(np.uint16)
+    rne = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert not np.array_equal(truncated, rne)
+    assert np.array_equal(O.f32_to_bf16(x), rne)
+
+    # a norm without the square root, or without the 1/N scale: the clip pin
+    gs = [(rng.standard_normal(64) * 0.3).astype(F32) for _ in range(3)]
+    tg = [torch.nn.Parameter(torch.zeros(64)) for _ in gs]
+    for t_, g_ in zip(tg, gs):
+        t_.grad = torch.from_numpy(g_.copy())
+    tnorm = float(torch.nn.utils.clip_grad_norm_(tg, 1.0, foreach=False))
+    norm, _ = O.grad_norm(gs, 1.0)
+    no_sqrt = sum(float(np.dot(g_.astype(np.float64), g_)) for g_ in gs)
+    assert abs(norm - tnorm) <= 1e-6 * tnorm and abs(no_sqrt - tnorm) > 1e-3 * tnorm
+
+    # the padding rounded down instead of up: the hand-derived tiny plan
+    numels, nr, al = [4096, 3000, 2904], 4, 16
+    floor_pad = (sum(numels) // (nr * al)) * nr * al
+    assert floor_pad != 10048 and O.plan(numels, nr, al).psi_pad == 10048
+
+    # the consumer's rounds as K**(rounds-1) instead of the geometric sum:
+    # the brute-force iteration pin
+    bits = rng.integers(0, 1 << 16, 24).astype(np.uint16)
+    M = 1 << 64
+    base = O.layer_checksum(bits, 1)
+    assert (base * pow(O.CONSUME_K, 2, M)) % M != O.layer_checksum(bits, 3)
+
+    # shards gathered in reverse owner order: the concatenation pin
+    shards = [rng.integers(0, 1 << 16, 5).astype(np.uint16) for _ in range(3)]
+    layer, _, _ = O.gather_layer(shards)
+    assert np.array_equal(layer, np.concatenate(shards))
+    assert not np.array_equal(layer, np.concatenate(shards[::-1]))
+
 
 def test_accumulation_over_micro_batches():
     # exact arithmetic: accumulating M micro-batches' reduce-scatters equals
