@@ -121,6 +121,58 @@ def test_checkpoint_resume_is_bit_exact(cuda):
     assert torch.equal(master, a.master) and torch.equal(m, a.m) and torch.equal(v, a.v)
 
 
+def test_stage3_step_with_gradient_clipping(cuda):
+    """Stage 3 with clipping by the global norm over all layer groups: a
+    norm-only reduce-scatter pass per group (partials into consecutive
+    slices), one device norm, then the per-group fused step with the device
+    coefficient writing the owners' shards.  Agrees with the oracle, which
+    takes the same global norm over all groups' scaled reduced gradients."""
+    import torch
+    d, ffn, vocab = 64, 172, 500
+    blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(2)]
+    numels = [vocab * d] + blocks[0] + blocks[1] + [d, vocab * d]
+    groups = [0] + [1] * 9 + [2] * 9 + [3, 3]
+    c = Case(numels, 8, 16, "bf16", grad_sigma=3e-3, seed=57, groups=groups, heavy_tail=True)
+    Z = c.Z
+    G = len(c.groups)
+    counts = [Z.zero_rs_partials(c.plan, Z.ZERO_BF16, g["psi_pad"]) for g in c.groups]
+    part = torch.zeros(sum(counts), dtype=torch.float64, device=cuda)
+    coef = torch.zeros(1, dtype=torch.float32, device=cuda)
+    norm = torch.zeros(1, dtype=torch.float32, device=cuda)
+    shards = [torch.zeros(c.info["shard_total"], dtype=torch.bfloat16, device=cuda)
+              for _ in range(8)]
+    grads = [c.grads_dev(gi, 1) for gi in range(G)]
+    off = 0
+    for gi, k in zip(range(G), counts):
+        Z.zero_reduce_scatter(c.plan, gi, grads[gi], Z.ZERO_BF16, None, 0,
+                              c.groups[gi]["psi_pad"], 1.0 / 8, part[off:off + k])
+        off += k
+    Z.zero_grad_norm(part, off, 1.0, norm, coef)
+    for gi in reversed(range(G)):
+        Z.zero_step_group(c.plan, gi, grads[gi], Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(1),
+                          coef, shards)
+    torch.cuda.synchronize()
+    # oracle: the same global norm, then each group's step with that coefficient
+    scaled = []
+    for gi, g in enumerate(c.groups):
+        red, _, _ = O.ring_reduce_scatter(c.grads_host(gi, 1), g["shard"])
+        scaled += O.scale(red, np.float32(1.0) / np.float32(8))
+    onorm, ocoef = O.grad_norm(scaled, 1.0)
+    assert float(ocoef) < 1.0                           # the clip is active
+    assert abs(norm.item() - onorm) <= 1e-6 * onorm
+    exact = coef.item() == float(ocoef)
+    for gi in reversed(range(G)):
+        c.oracle_step(gi, 1, clip_coef=ocoef)
+    c.check_state("stage 3 clipped", exact=exact)
+    for gi, g in enumerate(c.groups):
+        f0, S = g["flat_off"], g["shard"]
+        for k in range(8):
+            ro = g["rank_off"]
+            assert_bf16(bits_of(shards[k][ro:ro + S]),
+                        O.f32_to_bf16(c.h_master[f0 + k * S:f0 + (k + 1) * S]),
+                        f"shard {k} group {gi}", exact=exact)
+
+
 def test_occupancy_setting_does_not_change_results(cuda):
     """The resident-block cap only changes which thread handles which
     vector: element-wise outputs are bit-identical for every setting, and the
