@@ -806,6 +806,10 @@ def secondary_line(w, args, dist) -> dict:
                 "hbm_gbs_formula": formula / (ms * 1e-3) / 1e9,
                 "hbm_gbs_path": path / (ms * 1e-3) / 1e9,
                 "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind,
+                             "unit": "GB/s", "kernel": "rs_kernel + adam_kernel (the step)",
+                             "achieved": path / (ms * 1e-3) / 1e9,
+                             "frac": path / (ms * 1e-3) / 1e9 / peak,
+                             "traffic": None,
                              "rs_gbs": P * (gb * N + 4) / (r["rs_ms"] * 1e-3) / 1e9,
                              "adam_gbs": P * 30 / (r["adam_ms"] * 1e-3) / 1e9,
                              "rs_ms": r["rs_ms"], "adam_ms": r["adam_ms"], "norm_ms": r["norm_ms"]},
@@ -837,7 +841,11 @@ def secondary_line(w, args, dist) -> dict:
                        **({"schedule_graph_ms": r["graph_ms"],
                            "schedule_graph_gbs_incl_consumer": 6 * r["gather_elems"] /
                            (r["graph_ms"] * 1e-3) / 1e9} if r["graph_ms"] else {})},
-            "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind},
+            "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "kernel": "fused_kernel<16,bf16> (zero_step_group, 34 groups)",
+                         "achieved": algorithmic_bytes(N, P, 2) / (rs_ms * 1e-3) / 1e9,
+                         "frac": algorithmic_bytes(N, P, 2) / (rs_ms * 1e-3) / 1e9 / peak,
+                         "traffic": None},
             "clocks": r["clocks"]}
 
 
