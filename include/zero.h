@@ -285,6 +285,20 @@ int zero_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
               const float* d_coef, void* full_out, zero_dtype_t out_dtype,
               zero_stream_t stream);
 
+/* zero_step_acc: the last micro-batch of gradient accumulation ["ZeRO
+ * Optimizer", "Hybrid Approaches": gradient accumulation with
+ * micro-batching], fused: as zero_step, with the reduced gradient taken as
+ * accumulated[f] + (this micro-batch's ring sum), in that order, fp32 --
+ * `accumulated` being the flat fp32 buffer zero_reduce_scatter and
+ * zero_reduce_scatter_acc filled for the earlier micro-batches (read only).
+ * Bit-identical to zero_reduce_scatter_acc into that buffer followed by
+ * zero_adam_shard over the group, without storing and re-reading the reduced
+ * gradient (8 bytes per parameter less).  hp->grad_scale is 1/(N * micro-batches). */
+int zero_step_acc(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                  zero_dtype_t gdtype, const float* accumulated, float* master, float* m,
+                  float* v, const zero_adam_t* hp, const float* d_coef, void* full_out,
+                  zero_dtype_t out_dtype, zero_stream_t stream);
+
 /* zero_step_group (stage 3) [P4 "ZeRO Stages", stage 3]: as zero_step, but
  * each owner writes its updated bf16 parameters only into its own shard
  * buffer: shards[k][rank_off(g) + (i - k*S_g)] for owner k of element i. */

@@ -91,6 +91,47 @@ def test_gradient_accumulation_over_micro_batches(cuda):
     assert_bf16(bits_of(out), O.f32_to_bf16(p), "gathered")
 
 
+@pytest.mark.parametrize("gd", ["bf16", "f32"])
+def test_fused_last_micro_batch_equals_accumulate_then_adam(cuda, gd):
+    """zero_step_acc (the last micro-batch's ring sum added to the
+    accumulated buffer inside the fused step) equals zero_reduce_scatter_acc
+    followed by zero_adam_shard bit for bit, and the oracle's accumulation;
+    the accumulated buffer is left as it was."""
+    import torch
+    M = 3
+    a, b = (Case([70_001, 3_333, 17], 8, 16, gd, grad_sigma=1e-2 if gd == "f32" else 1e-3,
+                 seed=37) for _ in range(2))
+    Z = a.Z
+    P, S, N = a.info["psi_pad"], a.groups[0]["shard"], a.n
+    hp = Z.adam_hp(step=1, grad_scale=1.0 / (N * M))
+    acc_a = torch.empty(P, dtype=torch.float32, device=cuda)
+    grads = [a.grads_dev(0, 20 + k) for k in range(M)]
+    Z.zero_reduce_scatter(a.plan, 0, grads[0], a.zdtype, acc_a, 0, P, 1.0)
+    for k in range(1, M - 1):
+        Z.zero_reduce_scatter_acc(a.plan, 0, grads[k], a.zdtype, acc_a, 0, P, 1.0)
+    acc_b = acc_a.clone()
+    out_a = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    out_b = torch.empty(P, dtype=torch.bfloat16, device=cuda)
+    Z.zero_reduce_scatter_acc(a.plan, 0, grads[M - 1], a.zdtype, acc_a, 0, P, 1.0)
+    Z.zero_adam_shard(a.plan, 0, a.master, a.m, a.v, acc_a, hp, None, 0, P, out_a)
+    before = acc_b.clone()
+    Z.zero_step_acc(b.plan, 0, grads[M - 1], b.zdtype, acc_b, b.master, b.m, b.v, hp, None,
+                    out_b)
+    torch.cuda.synchronize()
+    assert torch.equal(acc_b, before)
+    for x, y, what in ((a.master, b.master, "master"), (a.m, b.m, "m"), (a.v, b.v, "v"),
+                       (out_a, out_b, "out")):
+        assert torch.equal(x, y), what
+    red = O.ring_reduce_scatter(a.grads_host(0, 20), S)[0]
+    for k in range(1, M):
+        red = O.accumulate_reduced(red, O.ring_reduce_scatter(a.grads_host(0, 20 + k), S)[0])
+    g = O.scale(red, np.float32(1.0 / (N * M)))
+    p, m, v = O.adam_update(b.h_master, b.h_m, b.h_v, np.concatenate(g), 1e-3, 0.9, 0.999, 1e-8,
+                            0.0, 1)
+    assert_close_f32(b.master.cpu().numpy(), p, "master")
+    assert_bf16(bits_of(out_b), O.f32_to_bf16(p), "gathered")
+
+
 def test_checkpoint_resume_is_bit_exact(cuda):
     """The optimizer state is three flat fp32 arrays plus the step number:
     dumping them to host memory after 3 steps and resuming in fresh buffers

@@ -126,6 +126,8 @@ _SIGS = {
                                   c_vp, c_vp, c_vp, c_i32, c_vp]),
     "zero_step": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp, P(zero_adam_t), c_vp,
                           c_vp, c_i32, c_vp]),
+    "zero_step_acc": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp, c_vp,
+                              P(zero_adam_t), c_vp, c_vp, c_i32, c_vp]),
     "zero_step_group": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp,
                                 P(zero_adam_t), c_vp, P(c_vp), c_vp]),
     "zero_gather_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
@@ -504,6 +506,20 @@ def zero_step(plan, group, grads, gdtype, master, m, v, hp, d_coef, full_out,
     _check(_lib().zero_step(plan, group, grad_ptrs, gdtype, _ptr(master), _ptr(m),
                             _ptr(v), ctypes.byref(hp), _ptr(d_coef), _ptr(full_out), out_dtype,
                             _stream(stream)), "zero_step")
+
+
+def zero_step_acc(plan, group, grads, gdtype, accumulated, master, m, v, hp, d_coef, full_out,
+                  out_dtype=ZERO_BF16, stream=None) -> None:
+    g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
+    if g is not None:
+        for x, what in ((accumulated, "accumulated"), (master, "master"), (m, "m"), (v, "v")):
+            _need(x, (g[0] + g[1]) * 4, what)
+        _need(full_out, (g[0] + g[1]) * _ESIZE.get(out_dtype, 0), "full_out")
+    _need(d_coef, 4, "d_coef")
+    grad_ptrs = _ranks(plan, grads, "grads", g[1] * es if g else 0)
+    _check(_lib().zero_step_acc(plan, group, grad_ptrs, gdtype, _ptr(accumulated), _ptr(master),
+                                _ptr(m), _ptr(v), ctypes.byref(hp), _ptr(d_coef),
+                                _ptr(full_out), out_dtype, _stream(stream)), "zero_step_acc")
 
 
 def zero_step_group(plan, group, grads, gdtype, master, m, v, hp, d_coef, shards,

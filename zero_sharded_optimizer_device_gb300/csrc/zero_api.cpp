@@ -333,11 +333,10 @@ extern "C" int zero_all_gather(const zero_plan_t* plan, int32_t group, const flo
   return cuda_status(zk::launch_cast(master, a, b, out_dtype, full_out, (cudaStream_t)stream));
 }
 
-extern "C" int zero_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
-                         zero_dtype_t gdtype, float* master, float* m, float* v,
-                         const zero_adam_t* hp, const float* d_coef, void* full_out,
-                         zero_dtype_t out_dtype, zero_stream_t stream) {
-  NvtxRange nvtx("zero_step");
+static int fused_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                      zero_dtype_t gdtype, const float* prev, float* master, float* m, float* v,
+                      const zero_adam_t* hp, const float* d_coef, void* full_out,
+                      zero_dtype_t out_dtype, zero_stream_t stream) {
   ZERO_TRY(check_group(plan, group));
   if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
   ZERO_TRY(check_rank_ptrs(plan, grads));
@@ -352,9 +351,29 @@ extern "C" int zero_step(const zero_plan_t* plan, int32_t group, const void* con
   const int mode = !full_out ? zk::OUT_NONE
                              : (out_dtype == ZERO_BF16 ? zk::OUT_FULL_BF16 : zk::OUT_FULL_F32);
   zk::OutPtrs none{};
-  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), fused_gdtype(plan, gdtype, grads), group_k(plan, group), 0,
-                                      plan->groups[group].psi_pad, master, m, v, k, d_coef, mode,
-                                      full_out, none, (cudaStream_t)stream));
+  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), fused_gdtype(plan, gdtype, grads),
+                                      group_k(plan, group), 0, plan->groups[group].psi_pad,
+                                      master, m, v, k, d_coef, prev, mode, full_out, none,
+                                      (cudaStream_t)stream));
+}
+
+extern "C" int zero_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                         zero_dtype_t gdtype, float* master, float* m, float* v,
+                         const zero_adam_t* hp, const float* d_coef, void* full_out,
+                         zero_dtype_t out_dtype, zero_stream_t stream) {
+  NvtxRange nvtx("zero_step");
+  return fused_step(plan, group, grads, gdtype, nullptr, master, m, v, hp, d_coef, full_out,
+                    out_dtype, stream);
+}
+
+extern "C" int zero_step_acc(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                             zero_dtype_t gdtype, const float* accumulated, float* master,
+                             float* m, float* v, const zero_adam_t* hp, const float* d_coef,
+                             void* full_out, zero_dtype_t out_dtype, zero_stream_t stream) {
+  NvtxRange nvtx("zero_step_acc");
+  ZERO_TRY(check_buf(accumulated));
+  return fused_step(plan, group, grads, gdtype, accumulated, master, m, v, hp, d_coef, full_out,
+                    out_dtype, stream);
 }
 
 extern "C" int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* grads,
@@ -375,7 +394,7 @@ extern "C" int zero_step_group(const zero_plan_t* plan, int32_t group, const voi
   zk::OutPtrs out{};
   for (int r = 0; r < plan->n_ranks; ++r) out.p[r] = shards[r];
   return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), fused_gdtype(plan, gdtype, grads), group_k(plan, group), 0,
-                                      plan->groups[group].psi_pad, master, m, v, k, d_coef,
+                                      plan->groups[group].psi_pad, master, m, v, k, d_coef, nullptr,
                                       zk::OUT_SHARDS_BF16, nullptr, out, (cudaStream_t)stream));
 }
 

@@ -76,9 +76,11 @@ cudaError_t launch_reduce_scatter(const RankPtrs& src, int gdtype, const GroupK&
                                   double* partials, int mode, cudaStream_t st);
 int64_t rs_partials_for(int n, int gdtype, int64_t n_elements);
 
+// prev (may be NULL): the fp32 reduced gradient accumulated over earlier
+// micro-batches, added before this one's ring sum (flat indices).
 cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64_t begin,
                          int64_t end, float* master, float* m, float* v, const AdamK& h,
-                         const float* coef, int out_mode, void* out_full,
+                         const float* coef, const float* prev, int out_mode, void* out_full,
                          const OutPtrs& shards, cudaStream_t st);
 
 cudaError_t launch_adam(const GroupK& g, int64_t begin, int64_t end, float* master, float* m,

@@ -189,8 +189,8 @@ template <int NT, typename GT>
 __global__ void __launch_bounds__(kThreads)
     fused_kernel(RankPtrs src, GroupK g, int64_t begin, int64_t end, float* __restrict__ master,
                  float* __restrict__ mom, float* __restrict__ var, AdamK h,
-                 const float* __restrict__ coef_ptr, int out_mode, void* __restrict__ out_full,
-                 OutPtrs shards) {
+                 const float* __restrict__ coef_ptr, const float* __restrict__ prev,
+                 int out_mode, void* __restrict__ out_full, OutPtrs shards) {
   const int n = NT > 0 ? NT : g.n;
   const float coef = coef_ptr ? *coef_ptr : 1.0f;
   if (h.bcp) {  // bias corrections kept on the device (graph-replayable steps)
@@ -215,6 +215,12 @@ __global__ void __launch_bounds__(kThreads)
       const float4 v0 = ld_state(var + f), v1 = ld_state(var + f + 4);
       float acc[8];
       ring_sum8<NT, GT>(src, n, k, i, acc);
+      if (prev) {  // gradient accumulation: earlier micro-batches first, then this one
+        const uint4 a = ld_once(prev + f), b = ld_once(prev + f + 4);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(__uint_as_float(w[e]), acc[e]);
+      }
       float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
       float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
       float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -260,7 +266,8 @@ __global__ void __launch_bounds__(kThreads)
             (out_mode == OUT_SHARDS_BF16 &&
              !in_extent(so, so + 1, g.rank_off, g.rank_off + g.S, ZERO_SITE_STEP_SHARD)))
           continue;
-        const float r = ring_sum1<GT>(src, n, kj, j);
+        float r = ring_sum1<GT>(src, n, kj, j);
+        if (prev) r = __fadd_rn(prev[f + e], r);
         float p = master[f + e], m = mom[f + e], v = var[f + e];
         adam1(p, m, v, scaled(r, h, coef), h);
         master[f + e] = p;
@@ -352,13 +359,14 @@ template <int NT, typename GT>
 struct FusedLaunch {
   static cudaError_t run(const RankPtrs& src, const GroupK& g, int64_t begin, int64_t end,
                          float* master, float* m, float* v, const AdamK& h, const float* coef,
-                         int out_mode, void* out_full, const OutPtrs& shards, cudaStream_t st) {
+                         const float* prev, int out_mode, void* out_full, const OutPtrs& shards,
+                         cudaStream_t st) {
     auto kern = fused_kernel<NT, GT>;
     const int64_t vecs = ((end + 7) >> 3) - (begin >> 3);
     const int nb = resident_blocks(kern, kThreads);
     const int cap = occupancy_cap(ZERO_OCC_FUSED);
     const int64_t grid = grid_for(vecs, kThreads, nb < cap ? nb : cap);
-    kern<<<(unsigned)grid, kThreads, 0, st>>>(src, g, begin, end, master, m, v, h, coef,
+    kern<<<(unsigned)grid, kThreads, 0, st>>>(src, g, begin, end, master, m, v, h, coef, prev,
                                                out_mode, out_full, shards);
     return cudaGetLastError();
   }
@@ -383,13 +391,13 @@ cudaError_t launch_reduce_scatter(const RankPtrs& src, int gdtype, const GroupK&
 
 cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64_t begin,
                          int64_t end, float* master, float* m, float* v, const AdamK& h,
-                         const float* coef, int out_mode, void* out_full,
+                         const float* coef, const float* prev, int out_mode, void* out_full,
                          const OutPtrs& shards, cudaStream_t st) {
   if (end <= begin) return cudaSuccess;
   if (gdtype == kF32Aligned32)
-    return dispatch_f32_wide<FusedLaunch>(g.n, src, g, begin, end, master, m, v, h, coef,
+    return dispatch_f32_wide<FusedLaunch>(g.n, src, g, begin, end, master, m, v, h, coef, prev,
                                           out_mode, out_full, shards, st);
-  return dispatch<FusedLaunch>(g.n, gdtype, src, g, begin, end, master, m, v, h, coef,
+  return dispatch<FusedLaunch>(g.n, gdtype, src, g, begin, end, master, m, v, h, coef, prev,
                                out_mode, out_full, shards, st);
 }
 
