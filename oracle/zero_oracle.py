@@ -29,8 +29,7 @@ arithmetic in fp32, one IEEE rounding per operation, in the order written
 below (numpy float32 ufuncs: no fused multiply-add, no reassociation).  The
 global gradient norm is accumulated in fp64.
 
-Readings where the pages leave a step open (each is listed with its reason in
-the design notes):
+Readings where the pages leave a step open:
   * flat buffer = the tensors concatenated in list order, padded only at the
     tail to a multiple of N*align; rank r owns [r*S, (r+1)*S)   [P2], [P1]
   * ring reduce-scatter: chunk k's partial sum starts at rank k+1 and travels
@@ -317,17 +316,32 @@ def scale(reduced, grad_scale):
     return [(x * s).astype(F32) for x in reduced]
 
 
-def grad_norm(g_chunks, max_norm: float):
-    """Global L2 norm of the scaled gradient, accumulated in fp64 over every
-    element in order, and the clip coefficient min(1, max_norm/(norm+1e-6))
-    rounded to fp32 (the coefficient torch.nn.utils.clip_grad_norm_ applies)."""
+def sum_squares(g_chunks) -> float:
+    """Sum of g*g over every element of the chunks, in fp64.  Each fp32 value
+    squares exactly in fp64 (a 24-bit significand squared needs at most 48
+    bits); the squares are added by ``np.dot`` per chunk and the chunk totals
+    in list order.  np.dot adds in blocks, not strictly left to right, so the
+    result is the exact sum up to fp64 rounding: a relative error of a few
+    times 1e-16 times the block depth, far below the fp32 rounding of the norm
+    that the callers compare."""
     acc = 0.0
     for x in g_chunks:
         d = x.astype(np.float64)
         acc += float(np.dot(d, d))
-    norm = float(np.sqrt(acc))
-    coef = min(1.0, float(max_norm) / (norm + 1e-6))
-    return norm, F32(coef)
+    return acc
+
+
+def clip_coef(norm: float, max_norm: float):
+    """min(1, max_norm / (norm + 1e-6)) in fp64, rounded to fp32 (the
+    coefficient torch.nn.utils.clip_grad_norm_ applies)."""
+    return F32(min(1.0, float(max_norm) / (float(norm) + 1e-6)))
+
+
+def grad_norm(g_chunks, max_norm: float):
+    """Global L2 norm of the scaled gradient, sqrt(sum_squares), and the clip
+    coefficient (clip_coef)."""
+    norm = float(np.sqrt(sum_squares(g_chunks)))
+    return norm, clip_coef(norm, max_norm)
 
 
 # ---------------------------------------------------------------------------
@@ -431,6 +445,42 @@ def gather_layer(rank_shards):
     and the per-rank counters."""
     fulls, sent, recv = ring_all_gather(rank_shards, len(rank_shards[0]))
     return fulls[0], sent, recv
+
+
+def broadcast_gather(rank_shards):
+    """Stage-3 gather of one layer group in the broadcast form ("Why does not
+    the stage 3 implementation use broadcast and reduce-scatter?", first
+    question and answer 1: the ZeRO paper broadcasts each owner's parameters,
+    DeepSpeed all-gathers them, at a similar communication volume).  N
+    broadcasts in rank order; in broadcast k the owner k sends its shard
+    straight to each of the other N - 1 ranks (the plain reading of a
+    broadcast from its root), and every rank places it at k*S of its layer
+    buffer.
+
+    Returns (rank 0's layer buffer, every rank's buffer, sent, received),
+    where sent[k][r] and received[k][r] count the elements rank r sent and
+    received in broadcast k."""
+    n = len(rank_shards)
+    sizes = [len(x) for x in rank_shards]
+    starts = np.cumsum([0] + sizes[:-1]).tolist()
+    have = [dict() for _ in range(n)]
+    sent = [[0] * n for _ in range(n)]
+    recv = [[0] * n for _ in range(n)]
+    for k in range(n):
+        have[k][k] = rank_shards[k]
+        for r in range(n):
+            if r == k:
+                continue
+            have[r][k] = rank_shards[k].copy()
+            sent[k][k] += sizes[k]
+            recv[k][r] += sizes[k]
+    fulls = []
+    for r in range(n):
+        full = np.empty(sum(sizes), dtype=rank_shards[0].dtype)
+        for c in range(n):
+            full[starts[c]:starts[c] + sizes[c]] = have[r][c]
+        fulls.append(full)
+    return fulls[0], fulls, sent, recv
 
 
 CONSUME_K = 6364136223846793005  # Knuth's MMIX LCG multiplier

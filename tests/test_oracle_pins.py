@@ -324,6 +324,49 @@ def test_gather_layer_is_concatenation_of_shards():
     assert sent == recv == [4 * 24] * 5
 
 
+def test_broadcast_gather_pins():
+    """Broadcast form of the stage-3 gather ("Why does not the stage 3
+    implementation use broadcast and reduce-scatter?", answer 1: broadcast
+    and all-gather move a similar volume): every rank ends with the
+    concatenation of the shards (brute force); in broadcast k only the root k
+    sends, (N - 1) * S elements, and every other rank receives S; summed over
+    the N broadcasts each rank sends and receives (N - 1) * S, the ring
+    all-gather's per-rank count."""
+    rng = np.random.default_rng(17)
+    for n, S in [(1, 7), (2, 5), (5, 24), (16, 3)]:
+        shards = [rng.integers(0, 1 << 16, S).astype(np.uint16) for _ in range(n)]
+        layer, fulls, sent, recv = O.broadcast_gather(shards)
+        cat = np.concatenate(shards)
+        assert np.array_equal(layer, cat)
+        assert all(np.array_equal(f, cat) for f in fulls)
+        for k in range(n):
+            assert sent[k] == [(n - 1) * S if r == k else 0 for r in range(n)]
+            assert recv[k] == [0 if r == k else S for r in range(n)]
+        _, ag_sent, ag_recv = O.gather_layer(shards)
+        assert [sum(sent[k][r] for k in range(n)) for r in range(n)] == ag_sent
+        assert [sum(recv[k][r] for k in range(n)) for r in range(n)] == ag_recv
+    # fp32 shards pass through bit for bit (NaN payloads included)
+    x = [np.array([np.nan, -0.0, 1e-45], dtype=F32), np.array([np.inf, 2.5, -1.0], dtype=F32)]
+    layer, _, _, _ = O.broadcast_gather(x)
+    assert np.array_equal(layer.view(np.uint32), np.concatenate(x).view(np.uint32))
+
+
+def test_sum_squares_is_the_exact_sum():
+    """fp32 squares are exact in fp64; on values whose squares and partial
+    sums are all exactly representable the sum is exact, and on random
+    values it is within fp64 rounding of math.fsum's correctly rounded sum."""
+    import math
+    rng = np.random.default_rng(18)
+    ints = [rng.integers(-1000, 1000, 300).astype(F32) for _ in range(3)]
+    want = sum(int(v) ** 2 for c in ints for v in c)
+    assert O.sum_squares(ints) == float(want)
+    xs = [(rng.standard_normal(5000) * 10.0 ** rng.integers(-8, 4, 5000)).astype(F32)
+          for _ in range(4)]
+    exact = math.fsum(float(v) * float(v) for c in xs for v in c)
+    assert abs(O.sum_squares(xs) - exact) <= 1e-13 * exact
+    assert O.clip_coef(math.sqrt(exact), 1.0) == O.grad_norm(xs, 1.0)[1]
+
+
 def test_layer_checksum_small_case():
     bits = np.array([1, 2, 3], dtype=np.uint16)
     assert O.layer_checksum(bits) == 1 * 1 + 2 * 2 + 3 * 3
