@@ -1,13 +1,21 @@
 """Benchmark of the ZeRO sharded-optimizer hot path on one GB300 per rank.
 
-Default workload: the GPT-2-small parameter list (124,439,808 parameters, 148
-tensors), N = 8 emulated data-parallel ranks, bf16 gradients, fp32 master /
-m / v, bf16 gathered parameters; one step = one fused zero_step (ring-order
-reduce-scatter + scale + Adam on every owner shard + all-gather).  Prints one
-JSON line (rank 0).
+Default workload: the Llama-7B stage-3 step -- 291 tensors, 6,738,415,616
+parameters in 34 layer groups (embedding, 32 transformer blocks, final norm +
+head), N = 16 emulated data-parallel ranks, bf16 gradients, fp32 master / m /
+v; one step = per layer group, in reverse order, the fused ring-order
+reduce-scatter + scale + Adam writing each owner's bf16 parameter shard
+(zero_step_group), 58 bytes per parameter.  The line also carries the
+per-layer gathers of the updated shards (alone, prefetched beside a consumer,
+and in the broadcast form) and the step end to end from host memory.  Prints
+one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload gpt2-small|gpt2-medium|llama-1.4b|llama-7b-stage3|tiny]
+                  [--workload llama-7b-stage3|gpt2-small|gpt2-medium|llama-1.4b|tiny]
+
+The other workloads: GPT-2-small (N = 8) and GPT-2-medium (N = 64, align 1)
+through the fused zero_step; Llama-1.4B (N = 8) through the bucketed
+reduce-scatter, global-norm clip and chunked Adam; tiny (N = 4).
 
 Under torchrun every rank runs an independent replica on its own GPU (the
 method shards nothing across GPUs here); value = all ranks' parameters
@@ -31,6 +39,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused ZeRO step Gparams/s and achieved HBM GB/s (% of peak), 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0       # GB300 HBM3e, nominal
+DEFAULT_WORKLOAD = "llama-7b-stage3"
 
 
 # ------------------------------------------------------------ distributed --
@@ -133,11 +143,20 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Where each measured kernel lives and which occupancy cap launches it.
+KERNEL_SOURCES = {"fused_kernel": ("zero_rs.cu", "ZERO_OCC_FUSED"),
+                  "rs_kernel": ("zero_rs.cu", "ZERO_OCC_RS"),
+                  "adam_kernel": ("zero_kernels.cu", "ZERO_OCC_ADAM"),
+                  "gather_bulk_kernel": ("zero_kernels.cu", "ZERO_OCC_GATHER")}
+
+
 def kernel_source_hash(kernel: str = "fused_kernel") -> str:
     """Hash of what decides a kernel's DRAM traffic: the device helpers, the
     kernel's own source text and its occupancy default (host code around it
     and the other kernels' defaults do not count)."""
-    return _source_hash(_read_csrc("zero_device.cuh"), _read_csrc("zero_rs.cu"), kernel)
+    fname, occ = KERNEL_SOURCES[kernel]
+    return _source_hash(_read_csrc("zero_device.cuh"), _read_csrc(fname), kernel,
+                        _read_csrc("zero_rs.cu"), occ)
 
 
 def _read_csrc(name: str) -> str:
@@ -145,38 +164,73 @@ def _read_csrc(name: str) -> str:
         return f.read()
 
 
-def _source_hash(device_h: str, rs_cu: str, kernel: str) -> str:
+def _source_hash(device_h: str, src: str, kernel: str, rs_cu: str = None,
+                 occ_kind: str = "ZERO_OCC_FUSED") -> str:
     h = hashlib.sha256()
     h.update(device_h.encode())
-    start = rs_cu.index(f"    {kernel}(")
-    start = rs_cu.rindex("template", 0, start)
-    end = rs_cu.index("// ------", start)
-    h.update(rs_cu[start:end].encode())
+    start = src.index(f"    {kernel}(")
+    start = src.rindex("template", 0, start)
+    end = src.index("// ------", start)
+    h.update(src[start:end].encode())
+    rs_cu = src if rs_cu is None else rs_cu
     occ = rs_cu.index("constexpr int kOccDefault")
     block = rs_cu[occ:rs_cu.index("};", occ)]
-    h.update(next(line for line in block.splitlines() if "ZERO_OCC_FUSED" in line).encode())
+    h.update(next(line for line in block.splitlines() if occ_kind in line).encode())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
+def profiled_traffic(kernel: str, workload: str, key: str = None):
     """DRAM bytes per launch from a committed ncu summary, only while the
-    kernel sources are unchanged since the capture."""
+    kernel sources are unchanged since the capture.  key: the record's name
+    under the workload (default: the kernel's)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    entry = rec.get(workload, {}).get(kernel)
+    entry = rec.get(workload, {}).get(key or kernel)
     if not entry or entry.get("source_hash") != kernel_source_hash(kernel):
         return None
     return entry.get("bytes_per_launch")
 
 
-def pinned_host_buffer(nbytes: int):
+def gpu_numa_node(dev_index: int):
+    """The host memory node nearest this GPU: its PCI device's NUMA node as
+    the kernel reports it (None when unknown or negative)."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(dev_index)
+        path = (f"/sys/bus/pci/devices/{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:"
+                f"{pr.pci_device_id:02x}.0/numa_node")
+        node = int(open(path).read().strip())
+    except (OSError, ValueError, AttributeError):
+        return None
+    return node if node >= 0 else None
+
+
+def _set_mempolicy(node):
+    """Bind this thread's future page allocations to one memory node (None:
+    back to the default policy).  Returns True on success."""
+    import ctypes
+    import platform
+    nr = {"aarch64": 237, "x86_64": 238}.get(platform.machine())
+    if nr is None:
+        return False
+    libc = ctypes.CDLL(None, use_errno=True)
+    if node is None:
+        return libc.syscall(nr, 0, None, 0) == 0                      # MPOL_DEFAULT
+    mask = (ctypes.c_ulong * 16)()
+    mask[node // 64] = 1 << (node % 64)
+    return libc.syscall(nr, 2, mask, 16 * 64) == 0                    # MPOL_BIND
+
+
+def pinned_host_buffer(nbytes: int, near_gpu: bool = False):
     """One page-locked host byte buffer of exactly nbytes from cudaHostAlloc
     (torch's pinned allocator would round each tensor up to a power of two).
-    Returns (uint8 tensor over it, function that frees it)."""
+    With near_gpu the pages are taken from the memory node nearest the
+    current GPU when the system reports one.  Returns (uint8 tensor over it,
+    function that frees it, description of the placement)."""
     import ctypes
     import torch
     rt = ctypes.CDLL("libcudart.so.13")
@@ -184,12 +238,21 @@ def pinned_host_buffer(nbytes: int):
     rt.cudaHostAlloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, ctypes.c_uint]
     rt.cudaFreeHost.restype = ctypes.c_int
     rt.cudaFreeHost.argtypes = [ctypes.c_void_p]
+    node = gpu_numa_node(torch.cuda.current_device()) if near_gpu else None
+    bound = node is not None and _set_mempolicy(node)
     ptr = ctypes.c_void_p()
-    rc = rt.cudaHostAlloc(ctypes.byref(ptr), nbytes, 0)
+    try:
+        rc = rt.cudaHostAlloc(ctypes.byref(ptr), nbytes, 0)
+    finally:
+        if bound:
+            _set_mempolicy(None)
     if rc != 0:
         raise RuntimeError(f"cudaHostAlloc of {nbytes} bytes failed ({rc})")
     t = torch.frombuffer((ctypes.c_uint8 * nbytes).from_address(ptr.value), dtype=torch.uint8)
-    return t, (lambda: rt.cudaFreeHost(ptr))
+    where = (f"pages bound to memory node {node}, the GPU's PCI NUMA node" if bound else
+             "default placement (the GPU reports no NUMA node)" if near_gpu and node is None else
+             "default placement")
+    return t, (lambda: rt.cudaFreeHost(ptr)), where
 
 
 def host_mapped(t) -> bool:
@@ -239,11 +302,12 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
     out = torch.empty(P, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     t = [0]
+    prepared = Z.prepare_zero_step(plan, 0, grads, zg, master, m, v, None, out, Z.ZERO_BF16,
+                                   stream)
 
     def step():
         t[0] += 1
-        Z.zero_step(plan, 0, grads, zg, master, m, v, Z.adam_hp(t[0], 1.0 / N), None, out,
-                    Z.ZERO_BF16, stream)
+        prepared(Z.adam_hp(t[0], 1.0 / N))
 
     for _ in range(warmup):
         step()
@@ -342,7 +406,7 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
                     h2d=N * P * gbytes, d2h=P * 2, e2e_steps=0,
                     e2e_transfer=f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
                                  f"exceeds 40% of the host's {ram / 1e9:.0f} GB")
-    pinned, free_pinned = pinned_host_buffer(host_bytes)
+    pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
     h_grads = [pinned[r * P * gbytes:(r + 1) * P * gbytes].view(gdt) for r in range(N)]
     for r in range(N):
         h_grads[r].copy_(grads[r])
@@ -385,7 +449,7 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
 
     return dict(local_ms=local_ms, launch_ms=launch_ms, e2e_ms=e2e_ms, psi=w.psi, psi_pad=P,
                 n_ranks=N, gbytes=gbytes, copy_gbs=copy_gbs, clocks=clocks.summary(),
-                h2d=N * P * gbytes, d2h=P * 2, e2e_steps=e2e_steps,
+                h2d=N * P * gbytes, d2h=P * 2, e2e_steps=e2e_steps, numa=numa,
                 e2e_transfer="zero-copy kernel access to mapped pinned host memory" if zero_copy
                 else "cudaMemcpyAsync from/to pinned host memory")
 
@@ -406,7 +470,7 @@ def _timed_launches(stream, calls):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def bench_bucketed(w, steps: int, warmup: int, dist: Dist) -> dict:
+def bench_bucketed(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = False) -> dict:
     """Reduce-scatter in fixed-size buckets with fp64 norm partials, global
     norm and clip coefficient on the device, Adam in chunks writing the bf16
     gathered parameters (the Llama-1.4B workload)."""
@@ -439,7 +503,7 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist) -> dict:
     stream = torch.cuda.current_stream(dev)
     t = [0]
 
-    def calls():
+    def calls(grads=grads, out=out):
         t[0] += 1
         hp = Z.adam_hp(t[0], 1.0 / N)
         cs = []
@@ -457,19 +521,75 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist) -> dict:
         for f in calls():
             f()
     torch.cuda.synchronize()
-    per_step, rs_ms, adam_ms, norm_ms = [], 0.0, 0.0, 0.0
+    nl = len(windows) + 1 + len(chunks)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
         dist.barrier()
-        for _ in range(steps):
-            ms = _timed_launches(stream, calls())
-            per_step.append(sum(ms))
-            rs_ms += sum(ms[:len(windows)])
-            norm_ms += ms[len(windows)]
-            adam_ms += sum(ms[len(windows) + 1:])
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(steps):
+            for j, f in enumerate(calls()):
+                evs[i][j].record(stream)
+                f()
+            evs[i][nl].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
         dist.barrier()
-    return dict(local_ms=statistics.fmean(per_step), rs_ms=rs_ms / steps, norm_ms=norm_ms / steps,
-                adam_ms=adam_ms / steps, P=P, N=N, n_launches=len(windows) + 1 + len(chunks),
-                clocks=clocks.summary(), norm=float(norm.item()), coef=float(coef.item()))
+    ms = [[e[j].elapsed_time(e[j + 1]) for j in range(nl)] for e in evs]
+    nw = len(windows)
+    res = dict(local_ms=t0.elapsed_time(t1) / steps,
+               rs_ms=statistics.fmean(sum(x[:nw]) for x in ms),
+               norm_ms=statistics.fmean(x[nw] for x in ms),
+               adam_ms=statistics.fmean(sum(x[nw + 1:]) for x in ms),
+               P=P, N=N, n_launches=nl, clocks=clocks.summary(), norm=float(norm.item()),
+               coef=float(coef.item()))
+
+    # end to end: gradients read from, and gathered parameters written to,
+    # page-locked host memory (zero-copy when mapped, else explicit copies)
+    gb = 2 if w.grad_dtype == "bf16" else 4
+    host_bytes = N * P * gb + P * 2
+    res.update(h2d=N * P * gb, d2h=P * 2, e2e_ms=None, e2e_steps=0)
+    if kernel_only:
+        return res
+    ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    if host_bytes > 0.4 * ram:
+        res["e2e_transfer"] = (f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
+                               f"exceeds 40% of the host's {ram / 1e9:.0f} GB")
+        return res
+    pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
+    h_grads = [pinned[r * P * gb:(r + 1) * P * gb].view(gdt) for r in range(N)]
+    h_out = pinned[N * P * gb:].view(torch.bfloat16)
+    for r in range(N):
+        h_grads[r].copy_(grads[r])
+    mapped = all(host_mapped(x) for x in h_grads + [h_out])
+
+    def e2e_step():
+        if mapped:
+            for f in calls(h_grads, h_out):
+                f()
+            return
+        for r in range(N):
+            grads[r].copy_(h_grads[r], non_blocking=True)
+        for f in calls():
+            f()
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = 3
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    res.update(e2e_ms=s0.elapsed_time(s1) / e2e_steps, e2e_steps=e2e_steps, numa=numa,
+               e2e_transfer="zero-copy kernel access to mapped pinned host memory" if mapped
+               else "cudaMemcpyAsync from/to pinned host memory")
+    del h_grads, h_out, pinned
+    free_pinned()
+    return res
 
 
 # ------------------------------------------- stage 3: step + per-layer gathers --
@@ -484,14 +604,18 @@ def _hidden(gathers_ms: float, consumers_ms: float, schedule_ms: float) -> float
     return (gathers_ms + consumers_ms - schedule_ms) / min(gathers_ms, consumers_ms)
 
 
-def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False) -> dict:
-    """Stage 3 (the Llama-7B workload): per layer group, in reverse order, a
-    fused reduce-scatter + Adam writing each owner's bf16 shard (gradients
-    regenerated into one slot per group, untimed); then every group gathered
-    into a contiguous layer buffer in forward and then reverse order, the
-    next group prefetched on a second stream while a consumer reads the
-    current one.  With ``use_graph`` the gather pass is also captured once in
-    a CUDA graph and its replay timed."""
+def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False,
+                 kernel_only: bool = False) -> dict:
+    """Stage 3 (the Llama-7B workload).  One step = per layer group, in
+    reverse order (the order backward produces them), the fused
+    reduce-scatter + scale + Adam writing each owner's bf16 shard
+    (zero_step_group).  Every group's N gradient buffers are prefixes of one
+    resident slot of N x (largest group) bf16 elements, filled once before
+    the clock starts (the full model's gradients, 216 GB at N = 16, do not
+    fit beside the state).  Then, untimed by the step: every group gathered
+    into a contiguous layer buffer in forward and then reverse order, alone,
+    in the two-stream prefetch schedule beside a consumer, and in the
+    broadcast form; and the step end to end from host memory."""
     import torch
     import synth
     import zero_sharded_optimizer_device_gb300 as Z
@@ -502,8 +626,10 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
     plan = Z.zero_plan(w.numels, N, w.align, w.groups)
     info = Z.zero_plan_info(plan)
     groups = [Z.zero_plan_group(plan, g) for g in range(info["n_groups"])]
+    G = len(groups)
     P, ST = info["psi_pad"], info["shard_total"]
-    gmax = max(g["psi_pad"] for g in groups)
+    big = max(range(G), key=lambda i: groups[i]["psi_pad"])
+    gmax = groups[big]["psi_pad"]
     master = torch.empty(P, dtype=torch.float32, device=dev)
     for g in groups:
         synth.fill_tensor(master[g["flat_off"]:g["flat_off"] + g["psi_pad"]], w.seed, synth.MASTER,
@@ -511,69 +637,116 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
     m, v = torch.zeros_like(master), torch.zeros_like(master)
     shards = [torch.zeros(ST, dtype=torch.bfloat16, device=dev) for _ in range(N)]
     slot = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(N)]
-    bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    sums = torch.zeros(2 * len(groups), dtype=torch.int64, device=dev)  # one per gather
+    gb = groups[big]
+    for r in range(N):
+        synth.fill_tensor(slot[r], w.seed, synth.GRAD, 1, r, gb["flat_off"], w.grad_sigma,
+                          gb["flat_off"] + gb["psi"])
+    views = [[t[:g["psi_pad"]] for t in slot] for g in groups]
     sa = torch.cuda.current_stream(dev)
+    rs_order = list(reversed(range(G)))
+    t = [0]
+
+    def step(grads=views, out=shards, stream=sa, events=None):
+        t[0] += 1
+        hp = Z.adam_hp(t[0], 1.0 / N)
+        for j, gi in enumerate(rs_order):
+            if events is not None:
+                events[j].record(stream)
+            Z.zero_step_group(plan, gi, grads[gi], Z.ZERO_BF16, master, m, v, hp, None, out,
+                              stream)
+        if events is not None:
+            events[G].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps; events between launches give each launch's time
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(G + 1)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0.record(sa)
+        for i in range(steps):
+            step(events=evs[i])
+        t1.record(sa)
+        torch.cuda.synchronize()
+        dist.barrier()
+    local_ms = t0.elapsed_time(t1) / steps
+    per_launch = [[e[j].elapsed_time(e[j + 1]) for j in range(G)] for e in evs]
+    launch_sum_ms = statistics.fmean(sum(x) for x in per_launch)
+    block = [j for j, gi in enumerate(rs_order) if 0 < gi < G - 1]     # transformer blocks
+    block_ms = statistics.fmean(x[j] for x in per_launch for j in block)
+    res = dict(local_ms=local_ms, launch_sum_ms=launch_sum_ms, block_ms=block_ms,
+               block_psi_pad=groups[1]["psi_pad"], P=P, N=N, groups=G, clocks=clocks.summary(),
+               launches_per_step=G)
+    if kernel_only:
+        return res
+
+    # copy-kernel peak of this GPU (context for the roofline denominator)
+    cbytes = 2 << 30
+    a = torch.empty(cbytes // 4, dtype=torch.float32, device=dev)
+    b = torch.empty_like(a)
+    for _ in range(3):
+        Z.zero_copy(b, a, cbytes, sa)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(sa)
+    for _ in range(10):
+        Z.zero_copy(b, a, cbytes, sa)
+    c1.record(sa)
+    torch.cuda.synchronize()
+    res["copy_gbs"] = 2 * cbytes * 10 / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    del a, b
+
+    res.update(_stage3_gathers(Z, plan, groups, shards, dev, sa, steps, use_graph))
+    res.update(_stage3_e2e(Z, plan, groups, N, ST, slot, master, m, v, sa, t))
+    return res
+
+
+def _stage3_gathers(Z, plan, groups, shards, dev, sa, steps, use_graph) -> dict:
+    """Forward + reverse per-group gathers of the updated bf16 shards: alone,
+    in the two-stream prefetch schedule beside the stand-in consumer (one
+    round: memory-bound; ARITH_ROUNDS: compute-bound), replayed from a CUDA
+    graph, and in the broadcast form (zero_broadcast_layer)."""
+    import torch
+    G = len(groups)
+    gmax = max(g["psi_pad"] for g in groups)
+    bufs = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    sums = torch.zeros(2 * G, dtype=torch.int64, device=dev)
     sb = torch.cuda.Stream(dev)
+    order = list(range(G)) + list(reversed(range(G)))
 
-    def fill(gi, step):
-        g = groups[gi]
-        for r in range(N):
-            synth.fill_tensor(slot[r][:g["psi_pad"]], w.seed, synth.GRAD, step, r, g["flat_off"],
-                              w.grad_sigma, g["flat_off"] + g["psi"])
-
-    def rs_adam_step(step):
-        ms = 0.0
-        for gi in reversed(range(len(groups))):
-            fill(gi, step)
-            ms += _timed_launches(sa, [lambda gi=gi: Z.zero_step_group(
-                plan, gi, slot, Z.ZERO_BF16, master, m, v, Z.adam_hp(step, 1.0 / N), None,
-                shards, sa)])[0]
-        return ms
-
-    order = list(range(len(groups))) + list(reversed(range(len(groups))))
-
-    def gather_schedule(rounds):
-        """Prefetch on stream B into the free buffer, consume on stream A
-        (the library's native two-stream schedule)."""
+    def timed(f):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(sa)
-        Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, rounds, sa, sb)
+        f()
         e1.record(sa)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
-    def consumers_only(rounds):
-        calls = [lambda j=j, gi=gi: Z.zero_layer_checksum(bufs[j % 2], groups[gi]["psi_pad"],
-                                                          rounds, sums[j:j + 1], sa)
-                 for j, gi in enumerate(order)]
-        return sum(_timed_launches(sa, calls))
+    def schedule(rounds):
+        return lambda: Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, rounds,
+                                                 sa, sb)
 
-    def gathers_only():
-        calls = [lambda j=j, gi=gi: Z.zero_gather_layer(plan, gi, shards, Z.ZERO_BF16,
-                                                        bufs[j % 2], sa)
-                 for j, gi in enumerate(order)]
-        return sum(_timed_launches(sa, calls))
+    def consumers(rounds):
+        def f():
+            for j, gi in enumerate(order):
+                Z.zero_layer_checksum(bufs[j % 2], groups[gi]["psi_pad"], rounds, sums[j:j + 1],
+                                      sa)
+        return f
 
-    def broadcasts_only():
-        """The ZeRO paper's broadcast form of the same gather: each owner in
-        turn sends its shard to every rank -- here one copy launch per owner
-        into the shared layer buffer instead of one all-gather kernel."""
-        calls = []
+    def gathers():
         for j, gi in enumerate(order):
-            g = groups[gi]
-            nbytes = g["shard"] * 2
-            for k in range(N):
-                src = shards[k].data_ptr() + g["rank_off"] * 2
-                dst = bufs[j % 2].data_ptr() + k * nbytes
-                calls.append(lambda s=src, d=dst, b=nbytes: Z.zero_copy(d, s, b, sa))
-        return sum(_timed_launches(sa, calls))
+            Z.zero_gather_layer(plan, gi, shards, Z.ZERO_BF16, bufs[j % 2], sa)
 
-    for s in range(1, warmup + 1):
-        rs_adam_step(s)
-        gather_schedule(1)
-        gather_schedule(ARITH_ROUNDS)
-    graph = None
+    def broadcasts():
+        for j, gi in enumerate(order):
+            Z.zero_broadcast_layer(plan, gi, shards, Z.ZERO_BF16, bufs[j % 2], sa)
+
+    runs = {"gathers_only_ms": gathers, "schedule_ms": schedule(1),
+            "schedule_arith_ms": schedule(ARITH_ROUNDS), "consumers_only_ms": consumers(1),
+            "consumers_arith_ms": consumers(ARITH_ROUNDS), "broadcast_ms": broadcasts}
     if use_graph:
         graph = torch.cuda.CUDAGraph()
         gs, gsb = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -583,40 +756,78 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
                 Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, 1, gs, gsb)
         sa.wait_stream(gs)
         torch.cuda.synchronize()
+        runs["schedule_graph_ms"] = graph.replay
+    for f in runs.values():           # warm-up
+        timed(f)
+    out = {k: statistics.fmean(timed(f) for _ in range(max(1, min(steps, 10))))
+           for k, f in runs.items()}
+    out["gather_elems"] = 2 * sum(g["psi_pad"] for g in groups)
+    out["gather_launches"] = len(order)
+    return out
 
-    def gather_schedule_graph():
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(sa)
-        graph.replay()
-        e1.record(sa)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
 
-    if graph is not None:
-        gather_schedule_graph()
-    rs_ms, sched_ms, gonly_ms, bcast_ms, graph_ms = [], [], [], [], []
-    cons_ms, sched_a_ms, cons_a_ms = [], [], []
-    with ClockSampler(dev.index) as clocks:
-        dist.barrier()
-        for s in range(warmup + 1, warmup + steps + 1):
-            rs_ms.append(rs_adam_step(s))
-            sched_ms.append(gather_schedule(1))
-            sched_a_ms.append(gather_schedule(ARITH_ROUNDS))
-            if graph is not None:
-                graph_ms.append(gather_schedule_graph())
-            gonly_ms.append(gathers_only())
-            cons_ms.append(consumers_only(1))
-            cons_a_ms.append(consumers_only(ARITH_ROUNDS))
-            bcast_ms.append(broadcasts_only())
-        dist.barrier()
-    gather_elems = 2 * sum(g["psi_pad"] for g in groups)
-    return dict(rs_ms=statistics.fmean(rs_ms), sched_ms=statistics.fmean(sched_ms),
-                gonly_ms=statistics.fmean(gonly_ms), bcast_ms=statistics.fmean(bcast_ms),
-                graph_ms=statistics.fmean(graph_ms) if graph_ms else None,
-                cons_ms=statistics.fmean(cons_ms), sched_a_ms=statistics.fmean(sched_a_ms),
-                cons_a_ms=statistics.fmean(cons_a_ms),
-                P=P, N=N, groups=len(groups),
-                gather_elems=gather_elems, clocks=clocks.summary())
+def _stage3_e2e(Z, plan, groups, N, ST, slot, master, m, v, sa, t) -> dict:
+    """The step end to end through the public API from host memory: the N
+    gradient buffers of each group in one page-locked host slot (N x largest
+    group, reused for every group, as the device slot is) and the owners'
+    bf16 shards written back to page-locked host buffers.  Mapped into the
+    device address space, zero_step_group reads and writes them over the host
+    link itself; otherwise explicit copies surround each group's step."""
+    import torch
+    G = len(groups)
+    gmax = slot[0].numel()
+    h2d = N * sum(g["psi_pad"] for g in groups) * 2
+    d2h = N * ST * 2
+    host_bytes = N * gmax * 2 + N * ST * 2
+    ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    base = dict(e2e_ms=None, h2d=h2d, d2h=d2h, e2e_steps=0)
+    if host_bytes > 0.4 * ram:
+        return dict(base, e2e_transfer=f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
+                                       f"exceeds 40% of the host's {ram / 1e9:.0f} GB")
+    pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
+    h_slot = [pinned[r * gmax * 2:(r + 1) * gmax * 2].view(torch.bfloat16) for r in range(N)]
+    off = N * gmax * 2
+    h_shards = [pinned[off + r * ST * 2:off + (r + 1) * ST * 2].view(torch.bfloat16)
+                for r in range(N)]
+    for r in range(N):
+        h_slot[r].copy_(slot[r])
+    mapped = all(host_mapped(x) for x in h_slot + h_shards)
+    h_views = [[x[:g["psi_pad"]] for x in h_slot] for g in groups]
+    d_views = [[x[:g["psi_pad"]] for x in slot] for g in groups]
+    dshards = None if mapped else [torch.empty(ST, dtype=torch.bfloat16, device=master.device)
+                                   for _ in range(N)]
+
+    def e2e_step():
+        t[0] += 1
+        hp = Z.adam_hp(t[0], 1.0 / N)
+        for gi in reversed(range(G)):
+            if mapped:
+                Z.zero_step_group(plan, gi, h_views[gi], Z.ZERO_BF16, master, m, v, hp, None,
+                                  h_shards, sa)
+            else:
+                for r in range(N):
+                    d_views[gi][r].copy_(h_views[gi][r], non_blocking=True)
+                Z.zero_step_group(plan, gi, d_views[gi], Z.ZERO_BF16, master, m, v, hp, None,
+                                  dshards, sa)
+        if not mapped:
+            for r in range(N):
+                h_shards[r].copy_(dshards[r], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    steps = 3
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(sa)
+    for _ in range(steps):
+        e2e_step()
+    s1.record(sa)
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / steps
+    del h_slot, h_shards, h_views, pinned
+    free_pinned()
+    return dict(base, e2e_ms=ms, e2e_steps=steps, numa=numa,
+                e2e_transfer="zero-copy kernel access to mapped pinned host memory" if mapped
+                else "cudaMemcpyAsync from/to pinned host memory")
 
 
 # ------------------------------------------- stage-3 gather granularity sweep --
@@ -718,39 +929,62 @@ def bench_gather_sweep(w, steps: int, dist: Dist, only=None) -> dict:
 
 
 # ------------------------------------------------- oracle on the host cores --
+def workload_kind(w) -> str:
+    if w.name.startswith("llama-1.4b"):
+        return "bucketed"
+    if w.groups is not None:
+        return "stage3"
+    return "fused"
+
+
 def oracle_sample(w, target_s: float, max_steps: int | None = None, window: int | None = None):
-    """Time the CPU oracle's fused step on a window of the workload that
-    straddles the boundary between owners 0 and 1; inputs generated before
-    the clock starts.  Returns (params per second, description, steps)."""
+    """Time the CPU oracle's step on a window of the workload that straddles
+    the boundary between owners 0 and 1 (stage 3: of the first transformer
+    block's group); inputs generated before the clock starts.  The bucketed
+    workload's step adds the global norm of the window and its clip.
+    Returns (params per second, description, steps, seconds)."""
     import numpy as np
     import synth
     from oracle import zero_oracle as O
 
     pin_to_one_core()
-    p = O.plan(w.numels, w.n_ranks, w.align)
-    S = p.groups[0].shard
-    win = window or min(p.psi_pad, 1 << 20)
-    a = max(0, min(S - win // 2, p.psi_pad - win))
+    kind = workload_kind(w)
+    p = O.plan(w.numels, w.n_ranks, w.align, w.groups)
+    gi = 1 if kind == "stage3" else 0
+    g = p.groups[gi]
+    S = g.shard
+    win = min(g.psi_pad, window or (1 << 20))
+    a = max(0, min(S - win // 2, g.psi_pad - win))
     b = a + win
     sdt = synth.DTYPE_BF16 if w.grad_dtype == "bf16" else synth.DTYPE_F32
+    fo = g.flat_off
     local = []
     for r in range(w.n_ranks):
-        x = synth.values(w.seed, synth.GRAD, 1, r, a, b, w.grad_sigma, w.psi, w.heavy_tail, sdt)
+        x = synth.values(w.seed, synth.GRAD, 1, r, fo + a, fo + b, w.grad_sigma, fo + g.psi,
+                         w.heavy_tail, sdt)
         local.append(O.bf16_to_f32(x) if sdt == synth.DTYPE_BF16 else x)
-    master = synth.values(w.seed, synth.MASTER, 0, 0, a, b, w.master_sigma, w.psi)
+    master = synth.values(w.seed, synth.MASTER, 0, 0, fo + a, fo + b, w.master_sigma, fo + g.psi)
     m = np.zeros_like(master)
     v = np.zeros_like(master)
     hp = O.AdamHP()
+    inv_n = np.float32(1.0) / np.float32(w.n_ranks)
     steps = 0
     t0 = time.perf_counter()
     while True:
         steps += 1
-        r = O.zero_step(local, master, m, v, S, steps, hp, window=(a, b))
+        coef = None
+        if kind == "bucketed":
+            red, _, _ = O.ring_reduce_scatter(local, S, (a, b))
+            _, coef = O.grad_norm(O.scale(red, inv_n), w.extra["max_norm"])
+        r = O.zero_step(local, master, m, v, S, steps, hp, window=(a, b), clip_coef=coef)
         master, m, v = r["master"], r["m"], r["v"]
         el = time.perf_counter() - t0
         if (max_steps and steps >= max_steps) or (not max_steps and el >= target_s):
             break
-    desc = (f"oracle fused step on elements [{a},{b}) of {w.name} (N={w.n_ranks}, owner 0/1 "
+    where = f"group {gi} " if kind == "stage3" else ""
+    what = {"fused": "fused step", "bucketed": "step with global-norm clip",
+            "stage3": "stage-3 group step"}[kind]
+    desc = (f"oracle {what} on elements [{a},{b}) of {where}{w.name} (N={w.n_ranks}, owner 0/1 "
             f"boundary), {steps} steps, single-threaded numpy")
     return win * steps / el, desc, steps, el
 
@@ -775,6 +1009,22 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
+def cpu_baseline(w) -> dict:
+    """The oracle, as it stands, timed for about 12 s on one host core."""
+    rate, desc, _, _ = oracle_sample(w, 12.0)
+    return {"value": rate / 1e9, "unit": "Gparams/s", "cores": 1, "kind": "oracle",
+            "sample": desc, "cpu": cpu_model(), "nproc": os.cpu_count()}
+
+
+def bucketed_bytes(w):
+    """(formula, path) bytes per step of the bucketed clipped workload: the
+    fused formula N*g + 26 per parameter, and what the clipped path moves --
+    the reduce-scatter's N*g + 4 (fp32 reduced gradient stored) and Adam's
+    4 + 24 + 2."""
+    gb = 2 if w.grad_dtype == "bf16" else 4
+    return algorithmic_bytes(w.n_ranks, w.psi, gb), w.psi * ((gb * w.n_ranks + 4) + 30)
+
+
 def fused_config(w, n_gpus: int) -> dict:
     """The `config` object both arms report for a fused-step workload."""
     abytes = algorithmic_bytes(w.n_ranks, w.psi, 2 if w.grad_dtype == "bf16" else 4)
@@ -786,82 +1036,218 @@ def fused_config(w, n_gpus: int) -> dict:
             "l2": f"inputs {abytes / 1e9:.2f} GB per step > L2 129 MB, no flush"}
 
 
-def secondary_line(w, args, dist) -> dict:
-    """JSON line for the bucketed and stage-3 workloads (not the headline)."""
-    peak, peak_kind = measured_hbm_peak()
+def workload_config(w, n_gpus: int) -> dict:
+    """The `config` object both arms report for any workload."""
+    kind = workload_kind(w)
+    if kind == "fused":
+        return fused_config(w, n_gpus)
+    common = {"psi": w.psi, "n_ranks": w.n_ranks, "align": w.align, "grad_dtype": w.grad_dtype,
+              "state": "fp32 master/m/v",
+              "parallelism": f"replicas x{n_gpus} (ranks emulated on each GPU)"}
+    if kind == "bucketed":
+        formula, path = bucketed_bytes(w)
+        return {"workload": f"{w.name} bucketed reduce-scatter (50M windows) + global-norm clip "
+                            "1.0 + Adam (200M chunks) + bf16 all-gather", **common,
+                "gathered": "bf16", "bytes_per_step": path, "bytes_per_step_formula": formula,
+                "l2": f"inputs {path / 1e9:.1f} GB per step > L2 129 MB, no flush"}
+    abytes = algorithmic_bytes(w.n_ranks, w.psi, 2 if w.grad_dtype == "bf16" else 4)
+    return {"workload": f"{w.name}: one stage-3 step = per layer group (34, reverse order) "
+                        "fused reduce-scatter + scale + Adam writing each owner's bf16 shard",
+            **common, "groups": len(set(w.groups)), "gathered": "bf16 owner shards",
+            "grads": "each group's N buffers are prefixes of one resident N x 202M bf16 slot",
+            "bytes_per_step": abytes,
+            "l2": f"inputs {abytes / 1e9:.0f} GB per step > L2 129 MB, no flush"}
+
+
+def _peaks() -> dict:
+    peak, kind = measured_hbm_peak()
+    return {"peak": peak, "peak_kind": kind, "peak_nominal_gbs": NOMINAL_HBM_GBS}
+
+
+# ------------------------------------------------------------------ lines --
+def fused_line(w, args, dist) -> dict:
+    res = bench_fused(w, args.steps, args.warmup, dist, args.kernel_only, args.graph,
+                      args.graph_steps)
+    ms = dist.max(res["local_ms"])
+    e2e_ms = dist.max(res["e2e_ms"]) if res["e2e_ms"] is not None else None
     n_gpus = dist.world
-    if w.name.startswith("llama-1.4b"):
-        r = bench_bucketed(w, args.steps, args.warmup, dist)
-        ms = dist.max(r["local_ms"])
-        P, N = r["P"], r["N"]
-        gb = 2 if w.grad_dtype == "bf16" else 4
-        formula = algorithmic_bytes(N, P, gb)             # N*gb + 26 B/param
-        path = P * ((gb * N + 4) + (4 + 24 + 2))          # RS N*gb+4, Adam 30
-        return {"metric": METRIC, "value": n_gpus * w.psi / (ms * 1e-3) / 1e9,
-                "unit": "Gparams/s", "n_gpus": n_gpus, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-                "scaling": "weak", "dtype": "f32", "data": "synthetic",
-                "config": {"workload": f"{w.name} bucketed RS (50M) + clip 1.0 + Adam (200M chunks)",
-                           "psi": w.psi, "n_ranks": N, "launches_per_step": r["n_launches"]},
-                "hbm_gbs_formula": formula / (ms * 1e-3) / 1e9,
-                "hbm_gbs_path": path / (ms * 1e-3) / 1e9,
-                "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind,
-                             "unit": "GB/s", "kernel": "rs_kernel + adam_kernel (the step)",
-                             "achieved": path / (ms * 1e-3) / 1e9,
-                             "frac": path / (ms * 1e-3) / 1e9 / peak,
-                             "traffic": None,
-                             "rs_gbs": P * (gb * N + 4) / (r["rs_ms"] * 1e-3) / 1e9,
-                             "adam_gbs": P * 30 / (r["adam_ms"] * 1e-3) / 1e9,
-                             "rs_ms": r["rs_ms"], "adam_ms": r["adam_ms"], "norm_ms": r["norm_ms"]},
-                "norm": r["norm"], "clip_coef": r["coef"], "clocks": r["clocks"],
-                "gpu_launches": r["n_launches"] * args.steps}
-    r = bench_stage3(w, args.steps, args.warmup, dist, args.graph)
+    value = n_gpus * w.psi / (ms * 1e-3) / 1e9
+    e2e_value = n_gpus * w.psi / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None
+    abytes = algorithmic_bytes(res["n_ranks"], res["psi_pad"], res["gbytes"])
+    pk = _peaks()
+    achieved = abytes / (res["launch_ms"] * 1e-3) / 1e9
+    step_gbs = abytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "Gparams/s", "n_gpus": n_gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": fused_config(w, n_gpus),
+        "hbm_gbs": step_gbs, "hbm_pct_of_peak": 100.0 * step_gbs / pk["peak"],
+        "roofline": {"bound": "hbm", "achieved": achieved, "unit": "GB/s",
+                     "frac": achieved / pk["peak"], **pk,
+                     "kernel": f"fused_kernel<{res['n_ranks']},{w.grad_dtype}>",
+                     "algorithmic_bytes_per_launch": abytes,
+                     "traffic": profiled_traffic("fused_kernel", w.name)},
+        "copy_peak_gbs": res["copy_gbs"],
+        "clocks": res["clocks"],
+        "e2e": {"value": e2e_value, "unit": "Gparams/s", "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"], "ms_per_step": e2e_ms,
+                "steps": res["e2e_steps"], "transfer": res.get("e2e_transfer"),
+                "host_memory": res.get("numa")},
+        "gpu_launches": 2 * args.steps if res.get("graph") else args.steps,
+    }
+    if res.get("graph"):
+        line["config"]["launch"] = (f"CUDA graph of {res['graph']} step(s), each an Adam state "
+                                    "advance + the fused kernel")
+    if args.kernel_only:
+        return {"kernel_only": True, "workload": w.name, "psi": w.psi, "ms_per_step": ms,
+                "value": value, "unit": "Gparams/s", "roofline": line["roofline"]}
+    return line
+
+
+def bucketed_line(w, args, dist) -> dict:
+    """JSON line of the clipped bucketed workload (Llama-1.4B)."""
+    r = bench_bucketed(w, args.steps, args.warmup, dist, args.kernel_only)
+    ms = dist.max(r["local_ms"])
+    P = r["P"]
+    N = r["N"]
+    gb = 2 if w.grad_dtype == "bf16" else 4
+    formula, path = bucketed_bytes(w)
+    pk = _peaks()
+    rs_bytes, adam_bytes = P * (gb * N + 4), P * 30
+    e2e_ms = dist.max(r["e2e_ms"]) if r["e2e_ms"] is not None else None
+    n_gpus = dist.world
+    line = {"metric": METRIC, "value": n_gpus * w.psi / (ms * 1e-3) / 1e9,
+            "unit": "Gparams/s", "n_gpus": n_gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(w, n_gpus), launches_per_step=r["n_launches"]),
+            "hbm_gbs_formula": formula / (ms * 1e-3) / 1e9,
+            "hbm_gbs_path": path / (ms * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", **pk, "unit": "GB/s",
+                         "kernel": "rs_kernel + norm_kernel + adam_kernel (the step)",
+                         "achieved": path / (ms * 1e-3) / 1e9,
+                         "frac": path / (ms * 1e-3) / 1e9 / pk["peak"],
+                         "frac_formula_42B": formula / (ms * 1e-3) / 1e9 / pk["peak"],
+                         "algorithmic_bytes_per_step": path,
+                         "traffic": _sum_or_none(
+                             profiled_traffic("rs_kernel", w.name, "rs_kernel_step"),
+                             profiled_traffic("adam_kernel", w.name, "adam_kernel_step")),
+                         "rs_gbs": rs_bytes / (r["rs_ms"] * 1e-3) / 1e9,
+                         "adam_gbs": adam_bytes / (r["adam_ms"] * 1e-3) / 1e9,
+                         "rs_ms": r["rs_ms"], "adam_ms": r["adam_ms"], "norm_ms": r["norm_ms"]},
+            "norm": r["norm"], "clip_coef": r["coef"], "clocks": r["clocks"],
+            "e2e": {"value": n_gpus * w.psi / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None,
+                    "unit": "Gparams/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"], "ms_per_step": e2e_ms,
+                    "steps": r["e2e_steps"], "transfer": r.get("e2e_transfer"),
+                    "host_memory": r.get("numa")},
+            "gpu_launches": r["n_launches"] * args.steps}
+    if args.kernel_only:
+        return {"kernel_only": True, "workload": w.name, "psi": w.psi, "ms_per_step": ms,
+                "value": line["value"], "unit": "Gparams/s", "roofline": line["roofline"]}
+    return line
+
+
+def _sum_or_none(*xs):
+    return None if any(x is None for x in xs) else sum(xs)
+
+
+def stage3_line(w, args, dist) -> dict:
+    """JSON line of the stage-3 workload (Llama-7B): the step, its roofline
+    on a transformer block's launch, the gathers, end to end."""
+    r = bench_stage3(w, args.steps, args.warmup, dist, args.graph, args.kernel_only)
     P, N = r["P"], r["N"]
-    rs_ms = dist.max(r["rs_ms"])
-    return {"metric": METRIC, "value": n_gpus * w.psi / (rs_ms * 1e-3) / 1e9,
+    ms = dist.max(r["local_ms"])
+    n_gpus = dist.world
+    pk = _peaks()
+    step_bytes = algorithmic_bytes(N, P, 2)
+    block_bytes = algorithmic_bytes(N, r["block_psi_pad"], 2)
+    achieved = block_bytes / (r["block_ms"] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "unit": "GB/s", "frac": achieved / pk["peak"],
+            **pk, "kernel": "fused_kernel<16,bf16> (zero_step_group), one transformer block's "
+                            "group per launch",
+            "algorithmic_bytes_per_launch": block_bytes,
+            "traffic": profiled_traffic("fused_kernel", w.name, "fused_kernel_block"),
+            "step_launches_gbs": step_bytes / (r["launch_sum_ms"] * 1e-3) / 1e9}
+    if args.kernel_only:
+        return {"kernel_only": True, "workload": w.name, "psi": w.psi, "ms_per_step": ms,
+                "value": n_gpus * w.psi / (ms * 1e-3) / 1e9, "unit": "Gparams/s",
+                "roofline": roof}
+    ge = r["gather_elems"]
+    gather = {"launches": r["gather_launches"],
+              "gathers_only_ms": r["gathers_only_ms"],
+              "gather_gbs": 4 * ge / (r["gathers_only_ms"] * 1e-3) / 1e9,
+              "gather_frac": 4 * ge / (r["gathers_only_ms"] * 1e-3) / 1e9 / pk["peak"],
+              "gather_traffic": profiled_traffic("gather_bulk_kernel", w.name,
+                                                 "gather_bulk_kernel_block"),
+              "broadcast_ms": r["broadcast_ms"],
+              "broadcast_gbs": 4 * ge / (r["broadcast_ms"] * 1e-3) / 1e9,
+              "schedule_ms": r["schedule_ms"],
+              "schedule_gbs_incl_consumer": 6 * ge / (r["schedule_ms"] * 1e-3) / 1e9,
+              "schedule_frac_incl_consumer": 6 * ge / (r["schedule_ms"] * 1e-3) / 1e9 / pk["peak"],
+              "consumers_only_ms": r["consumers_only_ms"],
+              "hidden": _hidden(r["gathers_only_ms"], r["consumers_only_ms"], r["schedule_ms"]),
+              "arith_consumer": {
+                  "rounds": ARITH_ROUNDS, "consumers_only_ms": r["consumers_arith_ms"],
+                  "schedule_ms": r["schedule_arith_ms"],
+                  "hidden": _hidden(r["gathers_only_ms"], r["consumers_arith_ms"],
+                                    r["schedule_arith_ms"])}}
+    if "schedule_graph_ms" in r:
+        gather["schedule_graph_ms"] = r["schedule_graph_ms"]
+    e2e_ms = dist.max(r["e2e_ms"]) if r["e2e_ms"] is not None else None
+    return {"metric": METRIC, "value": n_gpus * w.psi / (ms * 1e-3) / 1e9,
             "unit": "Gparams/s", "n_gpus": n_gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": rs_ms, "higher_is_better": True, "scaling": "weak", "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": f"{w.name}: per-group fused RS+Adam to owner shards, then "
-                                   "forward+reverse per-layer gathers prefetched on stream B",
-                       "psi": w.psi, "n_ranks": N, "groups": r["groups"]},
-            "rs_adam_gbs": algorithmic_bytes(N, P, 2) / (rs_ms * 1e-3) / 1e9,
-            "gather": {"schedule_ms": r["sched_ms"], "gathers_only_ms": r["gonly_ms"],
-                       "gather_gbs": 4 * r["gather_elems"] / (r["gonly_ms"] * 1e-3) / 1e9,
-                       "broadcast_ms": r["bcast_ms"],
-                       "broadcast_gbs": 4 * r["gather_elems"] / (r["bcast_ms"] * 1e-3) / 1e9,
-                       "schedule_gbs_incl_consumer": 6 * r["gather_elems"] /
-                       (r["sched_ms"] * 1e-3) / 1e9,
-                       "consumers_only_ms": r["cons_ms"],
-                       "hidden": _hidden(r["gonly_ms"], r["cons_ms"], r["sched_ms"]),
-                       "arith_consumer": {
-                           "rounds": ARITH_ROUNDS, "consumers_only_ms": r["cons_a_ms"],
-                           "schedule_ms": r["sched_a_ms"],
-                           "hidden": _hidden(r["gonly_ms"], r["cons_a_ms"], r["sched_a_ms"])},
-                       **({"schedule_graph_ms": r["graph_ms"],
-                           "schedule_graph_gbs_incl_consumer": 6 * r["gather_elems"] /
-                           (r["graph_ms"] * 1e-3) / 1e9} if r["graph_ms"] else {})},
-            "roofline": {"bound": "hbm", "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "kernel": "fused_kernel<16,bf16> (zero_step_group, 34 groups)",
-                         "achieved": algorithmic_bytes(N, P, 2) / (rs_ms * 1e-3) / 1e9,
-                         "frac": algorithmic_bytes(N, P, 2) / (rs_ms * 1e-3) / 1e9 / peak,
-                         "traffic": None},
-            "clocks": r["clocks"]}
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": workload_config(w, n_gpus),
+            "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
+            "hbm_pct_of_peak": 100.0 * step_bytes / (ms * 1e-3) / 1e9 / pk["peak"],
+            "roofline": roof, "copy_peak_gbs": r["copy_gbs"], "clocks": r["clocks"],
+            "gather": gather,
+            "e2e": {"value": n_gpus * w.psi / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None,
+                    "unit": "Gparams/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"], "ms_per_step": e2e_ms,
+                    "steps": r["e2e_steps"], "transfer": r.get("e2e_transfer"),
+                    "host_memory": r.get("numa")},
+            "gpu_launches": r["launches_per_step"] * args.steps}
 
 
 # -------------------------------------------------------------------- main --
+def reference_line(w, args, dist) -> dict:
+    """The reference arm: the CPU oracle, as it stands, on a bounded window
+    of the same workload per step (rank 0 only)."""
+    probe_rate, _, _, _ = oracle_sample(w, 0.0, max_steps=1, window=1 << 16)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    win = int(min(1 << 22, max(1 << 12, probe_rate * budget)))
+    win -= win % 16
+    if args.warmup:
+        oracle_sample(w, 0.0, max_steps=args.warmup, window=win)
+    rate, desc, steps, el = oracle_sample(w, 0.0, max_steps=args.steps, window=win)
+    value = rate / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "Gparams/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "Gparams/s", "cores": 1,
+                             "kind": "oracle", "sample": desc, "cpu": cpu_model()},
+            "e2e": {"value": value, "unit": "Gparams/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gpt2-small")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale", type=int, default=1,
                     help="shrink the workload's tensors by this factor (profiling cases)")
     ap.add_argument("--kernel-only", action="store_true",
-                    help="time only the step kernel: no copy peak, e2e or CPU baseline")
+                    help="time only the step kernels: no copy peak, gathers, e2e or CPU baseline")
     ap.add_argument("--graph", action="store_true",
                     help="replay one CUDA-graph-captured step (device-resident Adam step state); "
                          "stage-3 workload: also time the gather pass replayed from a graph")
@@ -886,28 +1272,8 @@ def main(argv=None):
     dist = Dist()
 
     if args.impl == "reference":
-        if dist.rank != 0:
-            dist.close()
-            return
-        # per step a bounded window, sized so warmup + steps stay ~2 minutes
-        probe_rate, _, _, _ = oracle_sample(w, 0.0, max_steps=1, window=1 << 16)
-        budget = 120.0 / max(1, args.steps + args.warmup)
-        win = int(min(1 << 22, max(1 << 12, probe_rate * budget)))
-        win -= win % 16
-        if args.warmup:
-            oracle_sample(w, 0.0, max_steps=args.warmup, window=win)
-        rate, desc, steps, el = oracle_sample(w, 0.0, max_steps=args.steps, window=win)
-        value = rate / 1e9
-        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "Gparams/s",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": el / steps * 1e3, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": fused_config(w, args.gpus),
-                "cpu_baseline": {"value": value, "unit": "Gparams/s", "cores": 1,
-                                 "kind": "oracle", "sample": desc, "cpu": cpu_model()},
-                "e2e": {"value": value, "unit": "Gparams/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
+        if dist.rank == 0:
+            print(json.dumps(reference_line(w, args, dist)), flush=True)
         dist.close()
         return
 
@@ -922,54 +1288,12 @@ def main(argv=None):
                               "n_ranks": w.n_ranks, "granularity": res}), flush=True)
         dist.close()
         return
-    if w.name.startswith("llama-1.4b") or w.name.startswith("llama-7b"):
-        line = secondary_line(w, args, dist)
-        if dist.rank == 0:
-            print(json.dumps(line), flush=True)
-        dist.close()
-        return
-
-    res = bench_fused(w, args.steps, args.warmup, dist, args.kernel_only, args.graph,
-                      args.graph_steps)
-    ms = dist.max(res["local_ms"])
-    e2e_ms = dist.max(res["e2e_ms"]) if res["e2e_ms"] is not None else None
-    n_gpus = dist.world
-    value = n_gpus * w.psi / (ms * 1e-3) / 1e9
-    e2e_value = n_gpus * w.psi / (e2e_ms * 1e-3) / 1e9 if e2e_ms else None
-    abytes = algorithmic_bytes(res["n_ranks"], res["psi_pad"], res["gbytes"])
-    peak, peak_kind = measured_hbm_peak()
-    achieved = abytes / (res["launch_ms"] * 1e-3) / 1e9
-    step_gbs = abytes / (ms * 1e-3) / 1e9
-    line = {
-        "metric": METRIC, "value": value, "unit": "Gparams/s", "n_gpus": n_gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": fused_config(w, n_gpus),
-        "hbm_gbs": step_gbs, "hbm_pct_of_peak": 100.0 * step_gbs / peak,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": f"fused_kernel<{res['n_ranks']},{w.grad_dtype}>",
-                     "algorithmic_bytes_per_launch": abytes,
-                     "traffic": profiled_traffic("fused_kernel", w.name)},
-        "copy_peak_gbs": res["copy_gbs"],
-        "clocks": res["clocks"],
-        "e2e": {"value": e2e_value, "unit": "Gparams/s", "h2d_bytes_per_step": res["h2d"],
-                "d2h_bytes_per_step": res["d2h"], "ms_per_step": e2e_ms,
-                "steps": res["e2e_steps"], "transfer": res.get("e2e_transfer")},
-        "gpu_launches": 2 * args.steps if res.get("graph") else args.steps,
-    }
-    if res.get("graph"):
-        line["config"]["launch"] = (f"CUDA graph of {res['graph']} step(s), each an Adam state "
-                                    "advance + the fused kernel")
-    if args.kernel_only:
-        line = {"kernel_only": True, "workload": w.name, "psi": w.psi, "ms_per_step": ms,
-                "value": value, "unit": "Gparams/s", "roofline": line["roofline"]}
-    elif dist.rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
-        rate, desc, steps, el = oracle_sample(w, 12.0)
-        line["cpu_baseline"] = {"value": rate / 1e9, "unit": "Gparams/s", "cores": 1,
-                                "kind": "oracle", "sample": desc, "cpu": cpu_model(),
-                                "nproc": os.cpu_count()}
+    kind = workload_kind(w)
+    line = {"fused": fused_line, "bucketed": bucketed_line, "stage3": stage3_line}[kind](
+        w, args, dist)
+    if (dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline
+            and not line.get("kernel_only")):
+        line["cpu_baseline"] = cpu_baseline(w)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()

@@ -293,7 +293,10 @@ int zero_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
  * zero_reduce_scatter_acc filled for the earlier micro-batches (read only).
  * Bit-identical to zero_reduce_scatter_acc into that buffer followed by
  * zero_adam_shard over the group, without storing and re-reading the reduced
- * gradient (8 bytes per parameter less).  hp->grad_scale is 1/(N * micro-batches). */
+ * gradient (8 bytes per parameter less).  hp->grad_scale is 1/(N * micro-batches).
+ * `accumulated` must not overlap master, m, v or full_out (the kernel reads it
+ * while writing those); the same pointer in two of these roles returns
+ * ZERO_EINVAL. */
 int zero_step_acc(const zero_plan_t* plan, int32_t group, const void* const* grads,
                   zero_dtype_t gdtype, const float* accumulated, float* master, float* m,
                   float* v, const zero_adam_t* hp, const float* d_coef, void* full_out,
@@ -318,6 +321,23 @@ int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* g
  * element. */
 int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
                       zero_dtype_t dtype, void* layer_out, zero_stream_t stream);
+
+/* zero_broadcast_layer (stage 3) ["Why does not the stage 3 implementation
+ * use broadcast and reduce-scatter?", first question and answer 1: the ZeRO
+ * paper's stage 3 sends each owner's parameters by broadcast; DeepSpeed
+ * gathers them with all-gather, at a similar communication volume]: the same
+ * layer buffer as zero_gather_layer, layer_out[j] = shards[j / S_g][rank_off(g)
+ * + j % S_g] for j in [0, psi_pad(g)), built the broadcast way: N broadcasts
+ * in rank order, broadcast k sending owner k's shard to every rank, i.e.
+ * writing layer_out[k*S_g, (k+1)*S_g).  Each broadcast is one kernel launch on
+ * `stream` (N launches per call: the N collectives of the broadcast form,
+ * each a separate step), by 1-D bulk copies when S_g and rank_off(g) are
+ * multiples of 16 bytes, element by element otherwise.  The result is
+ * bit-identical to zero_gather_layer's.  dtype: element type of the shard
+ * buffers (ZERO_BF16 or ZERO_F32); layer_out: psi_pad(g) elements,
+ * caller-owned.  Errors: EINVAL, EALIGN, ERANGE (group id), EDTYPE, ECUDA. */
+int zero_broadcast_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
+                         zero_dtype_t dtype, void* layer_out, zero_stream_t stream);
 
 /* zero_gather_groups (stage 3): zero_gather_layer for k groups at once:
  * layer_outs[i] receives group groups[i] (1 <= k <= ZERO_MAX_COALESCE; a
@@ -410,8 +430,12 @@ int zero_layer_checksum(const void* layer, int64_t n, int32_t rounds, uint64_t* 
  *     that exceeds ZERO_STATIC_PARTIALS the call returns ZERO_ERANGE and
  *     launches nothing.  (On a 152-SM GB300 any window needs at most a few
  *     hundred to 1216 slots.)
- *   - All calls share the slots; each call writes the slots it reads, so
- *     nothing needs clearing, but calls that overlap on the GPU race on them.
+ *   - The call fixes its reduce-scatter grid once and reads exactly the
+ *     slots that launch writes, so nothing needs clearing and a concurrent
+ *     zero_set_occupancy cannot make it read a slot it did not write.  An
+ *     empty window (begin == end) launches no reduce-scatter: norm 0,
+ *     coefficient 1.
+ *   - All calls share the slots: calls that overlap on the GPU race on them.
  * Errors: as zero_reduce_scatter and zero_grad_norm, plus ERANGE above. */
 #define ZERO_STATIC_PARTIALS 4096
 int zero_reduce_scatter_norm_static(const zero_plan_t* plan, int32_t group,

@@ -192,7 +192,8 @@ def test_random_calls_return_a_status_and_never_crash():
         elif which == 3:
             st = lib.zero_all_gather(p, g, addr(), addr(), dt, None)
         elif which == 4:
-            st = lib.zero_gather_layer(p, g, B._ptr_array(ptrs(n)), dt, addr(), None)
+            f = lib.zero_gather_layer if rng.integers(0, 2) else lib.zero_broadcast_layer
+            st = f(p, g, B._ptr_array(ptrs(n)), dt, addr(), None)
         elif which == 5:
             k = int(rng.integers(0, 4))
             grp = (B.c_i32 * max(1, k))(*[int(x) for x in rng.integers(-1, 3, k)])
@@ -218,6 +219,8 @@ def test_binding_refuses_pointer_lists_of_the_wrong_length():
         Z.zero_reduce_scatter(p, 0, [A, A, A], Z.ZERO_BF16, A, 0, 16, 0.25, None, 0)
     with pytest.raises(ValueError):
         Z.zero_gather_layer(p, 0, [A] * 5, Z.ZERO_BF16, A, 0)
+    with pytest.raises(ValueError):
+        Z.zero_broadcast_layer(p, 0, [A] * 3, Z.ZERO_BF16, A, 0)
     with pytest.raises(ValueError):
         Z.zero_gather_groups(p, [0, 0], [A] * 4, Z.ZERO_BF16, [A], 0)
     with pytest.raises(ValueError):
@@ -245,6 +248,11 @@ def test_binding_refuses_tensors_too_small_or_strided():
         Z.zero_all_gather(p, 0, ok, torch.zeros(100, dtype=torch.bfloat16), Z.ZERO_BF16, 0)
     with pytest.raises(ValueError, match="reduced: holds"):
         Z.zero_reduce_scatter(p, 0, g, Z.ZERO_BF16, small, 0, 1024, 0.25, None, 0)
+    # the prepared step checks the same buffers once, when prepared
+    with pytest.raises(ValueError, match="master: holds 4000 bytes"):
+        Z.prepare_zero_step(p, 0, g, Z.ZERO_BF16, small, ok, ok, None, None, Z.ZERO_BF16, 0)
+    with pytest.raises(ValueError, match=r"grads: 3 given"):
+        Z.prepare_zero_step(p, 0, g[:3], Z.ZERO_BF16, ok, ok, ok, None, None, Z.ZERO_BF16, 0)
 
 
 def test_plan_argument_errors():
@@ -306,6 +314,14 @@ def test_device_call_argument_errors_return_before_any_launch():
     assert status(Z.zero_adam_shard, p, 0, A, A, A, A, hp, None, 0, 200, None) == Z.ZERO_ERANGE
     assert status(Z.zero_all_gather, p, 3, A, A) == Z.ZERO_ERANGE
     assert status(Z.zero_gather_layer, p, 0, good, Z.ZERO_BF16, A + 1) == Z.ZERO_EALIGN
+    assert status(Z.zero_broadcast_layer, p, 0, good, Z.ZERO_BF16, A + 1) == Z.ZERO_EALIGN
+    assert status(Z.zero_broadcast_layer, p, 1, good, Z.ZERO_BF16, A) == Z.ZERO_ERANGE
+    assert status(Z.zero_broadcast_layer, p, 0, good, 3, A) == Z.ZERO_EDTYPE
+    assert status(Z.zero_broadcast_layer, p, 0, [A, A, 0, A], Z.ZERO_BF16, A) == Z.ZERO_EINVAL
+    assert status(Z.zero_step_acc, p, 0, good, Z.ZERO_BF16, A, A, A + 16, A + 32, hp, None,
+                  A + 48) == Z.ZERO_EINVAL                  # accumulated is also the master
+    assert status(Z.zero_step_acc, p, 0, good, Z.ZERO_BF16, A + 48, A, A + 16, A + 32, hp, None,
+                  A + 48) == Z.ZERO_EINVAL                  # ... or the output
     assert status(Z.zero_gather_groups, p, [0], good, Z.ZERO_BF16, [A + 2]) == Z.ZERO_EALIGN
     assert status(Z.zero_gather_groups, p, [0, 1], good, Z.ZERO_BF16, [A, A]) == Z.ZERO_ERANGE
     assert status(Z.zero_gather_groups, p, [], good, Z.ZERO_BF16, []) == Z.ZERO_EINVAL

@@ -28,7 +28,23 @@ def test_reference_arm_prints_the_contract_line():
     assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
-    assert d["config"] == bench.fused_config(W.GPT2_SMALL, 1)
+    assert d["config"] == bench.workload_config(W.LLAMA_7B_STAGE3, 1)
+    assert "llama-7b-stage3" in d["config"]["workload"]
+    assert d["config"]["bytes_per_step"] == bench.algorithmic_bytes(16, 6_738_415_616, 2)
+
+
+def test_reference_arm_of_each_workload_kind():
+    """The reference arm runs the oracle's step of every workload kind (fused,
+    bucketed with the clip, stage-3 group) and reports that workload's
+    config."""
+    for name in ("gpt2-small", "llama-1.4b"):
+        out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl",
+                              "reference", "--workload", name, "--steps", "1", "--warmup", "0"],
+                             capture_output=True, text=True, timeout=600, cwd=ROOT)
+        assert out.returncode == 0, out.stderr
+        d = json.loads(out.stdout.strip().splitlines()[-1])
+        assert d["config"] == bench.workload_config(W.ALL[name], 1)
+        assert d["value"] > 0 and name in d["cpu_baseline"]["sample"]
 
 
 def test_reference_arm_under_torchrun_prints_once():

@@ -311,8 +311,9 @@ def test_stage3_per_parameter_partitioning(cuda):
 
 def test_native_gather_schedule_matches_direct_gathers(cuda):
     """zero_stage3_gather_pass (gathers on stream B, consumer on stream A,
-    double-buffered) yields, for every gather of a forward + reverse pass,
-    the checksum of the directly gathered layer; and rejects bad input."""
+    double-buffered): for every gather of a forward + reverse pass the
+    consumer's checksum and the gathered buffer itself, element by element,
+    equal the oracle's all-gather of that layer; bad input is rejected."""
     import torch
     d, ffn, vocab = 64, 172, 500
     blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(3)]
@@ -333,13 +334,24 @@ def test_native_gather_schedule_matches_direct_gathers(cuda):
     Z.zero_stage3_gather_pass(c.plan, order, shards, bufs, gmax, sums, 1,
                               torch.cuda.current_stream(), sb)
     torch.cuda.synchronize()
-    for j, gi in enumerate(order):
+    host = [bits_of(t) for t in shards]
+    want = []
+    for gi in order:
         g = c.groups[gi]
-        layer = torch.empty(g["psi_pad"], dtype=torch.bfloat16, device=cuda)
-        Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, layer)
+        ro, S = g["rank_off"], g["shard"]
+        want.append(O.gather_layer([h[ro:ro + S] for h in host])[0])
+    for j, gi in enumerate(order):
+        assert int(sums[j].item()) % (1 << 64) == O.layer_checksum(want[j]), (j, gi)
+    # every gathered layer element by element: the pass over each prefix of
+    # the order leaves gather j in buffer j % 2 and gather j - 1 in the other
+    for j in range(len(order)):
+        Z.zero_stage3_gather_pass(c.plan, order[:j + 1], shards, bufs, gmax, sums, 1,
+                                  torch.cuda.current_stream(), sb)
         torch.cuda.synchronize()
-        bits = layer.cpu().view(torch.int16).numpy().view(np.uint16)
-        assert int(sums[j].item()) % (1 << 64) == O.layer_checksum(bits), (j, gi)
+        for i in (j, j - 1):
+            if i >= 0:
+                n_i = c.groups[order[i]]["psi_pad"]
+                assert np.array_equal(bits_of(bufs[i % 2][:n_i]), want[i]), (j, i)
     E = Z.ZeroError
     for bad, status in [(dict(order=[G]), Z.ZERO_ERANGE), (dict(buf_elems=10), Z.ZERO_ERANGE),
                         (dict(stream_b=torch.cuda.current_stream()), Z.ZERO_EINVAL),
@@ -357,8 +369,9 @@ def test_native_gather_schedule_matches_direct_gathers(cuda):
 def test_gather_pass_with_coalesced_steps(cuda):
     """Per-parameter partitioning with the two-stream pass: each step fetches
     one module's tensor groups together (zero_stage3_gather_pass_steps); the
-    consumer's checksum of every step equals the oracle's over the
-    concatenated gathered tensors, forward and reverse."""
+    consumer's checksum of every step, and the step's packed buffer element
+    by element, equal the oracle's concatenated gathered tensors, forward and
+    reverse."""
     import torch
     d, ffn, vocab = 64, 172, 500
     blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(3)]
@@ -377,17 +390,28 @@ def test_gather_pass_with_coalesced_steps(cuda):
     elems = [sum(c.groups[g]["psi_pad"] for g in st) for st in steps]
     bufs = [torch.empty(max(elems), dtype=torch.bfloat16, device=cuda) for _ in range(2)]
     sums = torch.zeros(len(steps), dtype=torch.int64, device=cuda)
+    sb = torch.cuda.Stream()
     Z.zero_stage3_gather_pass_steps(c.plan, steps, shards, bufs, max(elems), sums, 5,
-                                    torch.cuda.current_stream(), torch.cuda.Stream())
+                                    torch.cuda.current_stream(), sb)
     torch.cuda.synchronize()
+    want = []
     for j, st in enumerate(steps):
         parts = []
         for g in st:
             gi = c.groups[g]
-            want, _, _ = O.gather_layer([h[gi["rank_off"]:gi["rank_off"] + gi["shard"]]
-                                         for h in host])
-            parts.append(want)
-        assert int(sums[j].item()) % (1 << 64) == O.layer_checksum(np.concatenate(parts), 5), j
+            layer, _, _ = O.gather_layer([h[gi["rank_off"]:gi["rank_off"] + gi["shard"]]
+                                          for h in host])
+            parts.append(layer)
+        want.append(np.concatenate(parts))
+        assert int(sums[j].item()) % (1 << 64) == O.layer_checksum(want[j], 5), j
+    # every step's packed buffer element by element (pass over each prefix)
+    for j in range(len(steps)):
+        Z.zero_stage3_gather_pass_steps(c.plan, steps[:j + 1], shards, bufs, max(elems), sums, 1,
+                                        torch.cuda.current_stream(), sb)
+        torch.cuda.synchronize()
+        for i in (j, j - 1):
+            if i >= 0:
+                assert np.array_equal(bits_of(bufs[i % 2][:elems[i]]), want[i]), (j, i)
     E = Z.ZeroError
     with pytest.raises(E) as e:                           # a step must fit the buffers
         Z.zero_stage3_gather_pass_steps(c.plan, steps, shards, bufs, max(elems) - 1, sums, 1,
@@ -660,3 +684,31 @@ def test_fp32_gradient_load_paths_agree(cuda):
     for r in results[1:]:
         for a, b in zip(r, results[0]):
             assert torch.equal(a, b)
+
+
+def test_prepared_step_equals_zero_step(cuda):
+    """prepare_zero_step (buffers checked and marshalled once) launches the
+    same call as zero_step: three tiny steps through each give bit-identical
+    state and gathered parameters, equal to the oracle's."""
+    import torch
+    w = W.TINY
+    outs = []
+    for prepared in (False, True):
+        c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed)
+        Z = c.Z
+        out = torch.empty(c.info["psi_pad"], dtype=torch.bfloat16, device=cuda)
+        grads = c.grads_dev(0, 1)
+        step = Z.prepare_zero_step(c.plan, 0, grads, c.zdtype, c.master, c.m, c.v, None, out)
+        for s in range(1, 4):
+            c.grads_dev(0, s, grads)
+            if prepared:
+                step(c.hp_dev(s))
+            else:
+                Z.zero_step(c.plan, 0, grads, c.zdtype, c.master, c.m, c.v, c.hp_dev(s), None,
+                            out)
+            r = c.oracle_step(0, s)
+        torch.cuda.synchronize()
+        c.check_state(f"prepared={prepared}")
+        assert_bf16(bits_of(out), r["full"], "gathered")
+        outs.append((c.master.clone(), out.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])

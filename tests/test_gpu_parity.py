@@ -405,10 +405,12 @@ def test_stage3_outputs_stay_inside_their_buffers(cuda):
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("n,align", [(16, 16), (4, 8), (5, 4), (3, 3), (7, 1)])
 def test_gather_layer_every_path(cuda, dtype, n, align):
-    """zero_gather_layer on bf16 and fp32 shard buffers, through the bulk-copy
-    form (shard starts and lengths multiples of 16 bytes) and the element
-    form (otherwise): the layer is the concatenation of the owners' shards,
-    bit for bit, with guard bands around it."""
+    """zero_gather_layer and its broadcast form zero_broadcast_layer on bf16
+    and fp32 shard buffers, through the bulk-copy form (shard starts and
+    lengths multiples of 16 bytes) and the element form (otherwise): the
+    layer equals the oracle's all-gather and broadcast results (the
+    concatenation of the owners' shards), bit for bit, with guard bands
+    around it."""
     import torch
     rng = np.random.default_rng(1000 * n + align + (7 if dtype == "f32" else 0))
     numels = [int(x) for x in rng.integers(1, 40_000, 6)]
@@ -424,13 +426,46 @@ def test_gather_layer_every_path(cuda, dtype, n, align):
               for h in host]
     G = 64
     for gi, g in enumerate(p.groups):
-        buf = torch.full((g.psi_pad + 2 * G,), -7, dtype=tdt, device=cuda)
-        Z.zero_gather_layer(zp, gi, shards, zdt, buf[G:G + g.psi_pad])
-        torch.cuda.synchronize()
-        got = buf.cpu().numpy().view(ndt)
-        want, _, _ = O.gather_layer([h[g.rank_off:g.rank_off + g.shard] for h in host])
-        assert np.array_equal(got[G:G + g.psi_pad], want), (gi, n, align, dtype)
-        assert (buf[:G] == -7).all() and (buf[G + g.psi_pad:] == -7).all(), (gi, "guard")
+        own = [h[g.rank_off:g.rank_off + g.shard] for h in host]
+        want, _, _ = O.gather_layer(own)
+        want_b, _, _, _ = O.broadcast_gather(own)
+        for call, ref in ((Z.zero_gather_layer, want), (Z.zero_broadcast_layer, want_b)):
+            buf = torch.full((g.psi_pad + 2 * G,), -7, dtype=tdt, device=cuda)
+            call(zp, gi, shards, zdt, buf[G:G + g.psi_pad])
+            torch.cuda.synchronize()
+            got = buf.cpu().numpy().view(ndt)
+            assert np.array_equal(got[G:G + g.psi_pad], ref), (call.__name__, gi, n, align, dtype)
+            assert (buf[:G] == -7).all() and (buf[G + g.psi_pad:] == -7).all(), (gi, "guard")
+
+
+@pytest.mark.parametrize("n,pieces", [(2, 1), (2, 150), (3, 304), (16, 305), (16, 1000),
+                                      (5, 2999)])
+@pytest.mark.parametrize("ctas", [1, 2, 8])
+def test_bulk_gather_piece_walk(cuda, n, pieces, ctas):
+    """The bulk-copy gather's CTAs walk their pieces (8 KiB, every G-th) with
+    a cursor over owners and groups: per-owner piece counts below, at and
+    above the grid (1 to 8 CTAs per SM), a ragged last piece per owner, and
+    the broadcast form; every layer equals the plain concatenation of the
+    owners' shards (torch.cat), bit for bit."""
+    import torch
+    Z = pytest.importorskip("zero_sharded_optimizer_device_gb300")
+    S = pieces * 4096 - 8                        # bf16 elements per owner
+    zp = Z.zero_plan([n * S - 3, 3], n, 8)
+    assert Z.zero_plan_group(zp, 0)["shard"] == S
+    gen = torch.Generator(device=cuda).manual_seed(n * 7919 + pieces)
+    shards = [torch.randint(-32768, 32767, (S,), dtype=torch.int16, device=cuda, generator=gen)
+              for _ in range(n)]
+    want = torch.cat(shards)
+    prev = Z.zero_set_occupancy(Z.ZERO_OCC_GATHER, ctas)
+    try:
+        for call in (Z.zero_gather_layer, Z.zero_broadcast_layer):
+            out = torch.full((n * S + 64,), 5, dtype=torch.int16, device=cuda)
+            call(zp, 0, shards, Z.ZERO_BF16, out)
+            torch.cuda.synchronize()
+            assert torch.equal(out[:n * S], want), call.__name__
+            assert bool((out[n * S:] == 5).all())
+    finally:
+        Z.zero_set_occupancy(Z.ZERO_OCC_GATHER, prev)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])

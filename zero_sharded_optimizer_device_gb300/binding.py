@@ -131,6 +131,7 @@ _SIGS = {
     "zero_step_group": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp,
                                 P(zero_adam_t), c_vp, P(c_vp), c_vp]),
     "zero_gather_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
+    "zero_broadcast_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
     "zero_gather_groups": (c_i32, [c_vp, P(c_i32), c_i32, P(c_vp), c_i32, P(c_vp), c_vp]),
     "zero_layer_checksum": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp]),
     "zero_stage3_gather_pass": (c_i32, [c_vp, P(c_i32), c_i32, P(c_vp), P(c_vp), c_i64, c_vp,
@@ -508,6 +509,31 @@ def zero_step(plan, group, grads, gdtype, master, m, v, hp, d_coef, full_out,
                             _stream(stream)), "zero_step")
 
 
+def prepare_zero_step(plan, group, grads, gdtype, master, m, v, d_coef, full_out,
+                      out_dtype=ZERO_BF16, stream=None):
+    """zero_step with its buffers checked and marshalled once: returns a
+    function step(hp) that launches the same call with this step's Adam
+    hyperparameters.  For small, host-bound workloads, where the binding's
+    per-call checks cost more than the kernel.  The caller keeps every buffer
+    alive, in place and at its size while the function is used."""
+    g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
+    if g is not None:
+        for x, what in ((master, "master"), (m, "m"), (v, "v")):
+            _need(x, (g[0] + g[1]) * 4, what)
+        _need(full_out, (g[0] + g[1]) * _ESIZE.get(out_dtype, 0), "full_out")
+    _need(d_coef, 4, "d_coef")
+    grad_ptrs = _ranks(plan, grads, "grads", g[1] * es if g else 0)
+    head = (plan, group, grad_ptrs, gdtype, _ptr(master), _ptr(m), _ptr(v))
+    tail = (_ptr(d_coef), _ptr(full_out), out_dtype, _stream(stream))
+    f = _lib().zero_step
+
+    def step(hp) -> None:
+        _check(f(*head, ctypes.byref(hp), *tail), "zero_step")
+
+    step.keep = (grads, master, m, v, d_coef, full_out)   # the buffers stay referenced
+    return step
+
+
 def zero_step_acc(plan, group, grads, gdtype, accumulated, master, m, v, hp, d_coef, full_out,
                   out_dtype=ZERO_BF16, stream=None) -> None:
     g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
@@ -543,6 +569,15 @@ def zero_gather_layer(plan, group, shards, dtype, layer_out, stream=None) -> Non
     shard_ptrs = _ranks(plan, shards, "shards", plan.geometry()["shard_total"] * es)
     _check(_lib().zero_gather_layer(plan, group, shard_ptrs, dtype, _ptr(layer_out),
                                     _stream(stream)), "zero_gather_layer")
+
+
+def zero_broadcast_layer(plan, group, shards, dtype, layer_out, stream=None) -> None:
+    g, es = _group(plan, group), _ESIZE.get(dtype, 0)
+    if g is not None:
+        _need(layer_out, g[1] * es, "layer_out")
+    shard_ptrs = _ranks(plan, shards, "shards", plan.geometry()["shard_total"] * es)
+    _check(_lib().zero_broadcast_layer(plan, group, shard_ptrs, dtype, _ptr(layer_out),
+                                       _stream(stream)), "zero_broadcast_layer")
 
 
 def zero_gather_groups(plan, groups, shards, dtype, layer_outs, stream=None) -> None:

@@ -180,11 +180,10 @@ extern "C" int zero_rs_partials(const zero_plan_t* plan, zero_dtype_t gdtype, in
   return ZERO_OK;
 }
 
-extern "C" int zero_reduce_scatter(const zero_plan_t* plan, int32_t group,
-                                   const void* const* grads, zero_dtype_t gdtype, float* reduced,
-                                   int64_t begin, int64_t end, float grad_scale,
-                                   double* sumsq_partials, zero_stream_t stream) {
-  NvtxRange nvtx("zero_reduce_scatter");
+int zk::reduce_scatter_entry(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                             zero_dtype_t gdtype, float* reduced, int64_t begin, int64_t end,
+                             float grad_scale, double* sumsq_partials, int64_t grid,
+                             cudaStream_t stream) {
   ZERO_TRY(check_group(plan, group));
   if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
   ZERO_TRY(check_window(plan, group, begin, end));
@@ -194,7 +193,16 @@ extern "C" int zero_reduce_scatter(const zero_plan_t* plan, int32_t group,
   ZERO_TRY(check_opt_f64(sumsq_partials));
   return cuda_status(zk::launch_reduce_scatter(
       rank_ptrs(plan, grads), gdtype, group_k(plan, group), reduced, begin, end, grad_scale,
-      sumsq_partials, reduced ? zk::RS_STORE : zk::RS_NORM_ONLY, (cudaStream_t)stream));
+      sumsq_partials, reduced ? zk::RS_STORE : zk::RS_NORM_ONLY, stream, grid));
+}
+
+extern "C" int zero_reduce_scatter(const zero_plan_t* plan, int32_t group,
+                                   const void* const* grads, zero_dtype_t gdtype, float* reduced,
+                                   int64_t begin, int64_t end, float grad_scale,
+                                   double* sumsq_partials, zero_stream_t stream) {
+  NvtxRange nvtx("zero_reduce_scatter");
+  return zk::reduce_scatter_entry(plan, group, grads, gdtype, reduced, begin, end, grad_scale,
+                                  sumsq_partials, 0, (cudaStream_t)stream);
 }
 
 extern "C" int zero_reduce_scatter_acc(const zero_plan_t* plan, int32_t group,
@@ -372,6 +380,10 @@ extern "C" int zero_step_acc(const zero_plan_t* plan, int32_t group, const void*
                              void* full_out, zero_dtype_t out_dtype, zero_stream_t stream) {
   NvtxRange nvtx("zero_step_acc");
   ZERO_TRY(check_buf(accumulated));
+  // the kernel reads `accumulated` through a restrict pointer while it writes
+  // the state and the output: the same buffer in two roles is refused
+  const void* acc = accumulated;
+  if (acc == master || acc == m || acc == v || acc == full_out) return ZERO_EINVAL;
   return fused_step(plan, group, grads, gdtype, accumulated, master, m, v, hp, d_coef, full_out,
                     out_dtype, stream);
 }
@@ -408,6 +420,19 @@ extern "C" int zero_gather_layer(const zero_plan_t* plan, int32_t group, const v
   return cuda_status(zk::launch_gather(rank_ptrs(plan, shards), dtype == ZERO_BF16 ? 2 : 4,
                                        group_k(plan, group), plan->groups[group].psi_pad,
                                        layer_out, ZERO_OCC_GATHER, (cudaStream_t)stream));
+}
+
+extern "C" int zero_broadcast_layer(const zero_plan_t* plan, int32_t group,
+                                    const void* const* shards, zero_dtype_t dtype,
+                                    void* layer_out, zero_stream_t stream) {
+  NvtxRange nvtx("zero_broadcast_layer");
+  ZERO_TRY(check_group(plan, group));
+  if (!dtype_ok(dtype)) return ZERO_EDTYPE;
+  ZERO_TRY(check_rank_ptrs(plan, shards));
+  ZERO_TRY(check_buf(layer_out));
+  return cuda_status(zk::launch_broadcast(rank_ptrs(plan, shards), dtype == ZERO_BF16 ? 2 : 4,
+                                          group_k(plan, group), layer_out, ZERO_OCC_GATHER,
+                                          (cudaStream_t)stream));
 }
 
 extern "C" int zero_gather_groups(const zero_plan_t* plan, const int32_t* groups, int32_t k,

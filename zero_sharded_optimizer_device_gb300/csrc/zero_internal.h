@@ -71,10 +71,20 @@ enum RsMode : int {
 };
 
 // Launchers (zero_kernels.cu, zero_rs.cu).  Each returns the launch status.
+// grid > 0 fixes the launch's block count (and so the number of partials it
+// writes); 0 takes the default one-wave grid of rs_partials_for().
 cudaError_t launch_reduce_scatter(const RankPtrs& src, int gdtype, const GroupK& g,
                                   float* reduced, int64_t begin, int64_t end, float scale,
-                                  double* partials, int mode, cudaStream_t st);
+                                  double* partials, int mode, cudaStream_t st,
+                                  int64_t grid = 0);
 int64_t rs_partials_for(int n, int gdtype, int64_t n_elements);
+
+// zero_reduce_scatter's checks and launch with the grid fixed by the caller
+// (see launch_reduce_scatter).
+int reduce_scatter_entry(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                         zero_dtype_t gdtype, float* reduced, int64_t begin, int64_t end,
+                         float grad_scale, double* sumsq_partials, int64_t grid,
+                         cudaStream_t stream);
 
 // prev (may be NULL): the fp32 reduced gradient accumulated over earlier
 // micro-batches, added before this one's ring sum (flat indices).
@@ -99,6 +109,11 @@ cudaError_t launch_norm(const double* partials, int64_t n, float max_norm, float
 cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
                           int64_t psi_pad, void* out, int occ_kind, cudaStream_t st);
 
+// Broadcast form of the same gather: N launches, launch k copying owner k's
+// shard of the group to out[k*S, (k+1)*S) (one launch per broadcast root).
+cudaError_t launch_broadcast(const RankPtrs& shards, int elem_bytes, const GroupK& g, void* out,
+                             int occ_kind, cudaStream_t st);
+
 // Groups gathered by one bulk-copy launch (kernel parameter, by value).
 struct BulkGroups {
   int ng;  // groups in use
@@ -115,8 +130,10 @@ void bulk_add(BulkGroups& bg, int64_t S, int64_t rank_off, void* out);
 cudaError_t launch_gather_bulk(const RankPtrs& shards, const BulkGroups& bg, int occ_kind,
                                cudaStream_t st);
 
+// clear: zero *out first (false: the caller has zeroed it, e.g. once for all
+// the consumers of a gather pass).
 cudaError_t launch_checksum(const void* layer, int64_t n, int rounds, uint64_t* out,
-                            cudaStream_t st);
+                            cudaStream_t st, bool clear = true);
 
 cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t st);
 

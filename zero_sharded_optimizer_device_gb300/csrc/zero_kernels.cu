@@ -5,6 +5,8 @@
 //   gather_bulk_kernel / gather_kernel  stage-3 per-layer gather of N rank shards
 //   checksum_kernel consumer of a gathered layer (stands in for its computation)
 //   copy_kernel     16-byte device copy (achievable HBM bandwidth)
+#include <atomic>
+
 #include "zero_device.cuh"
 
 namespace zk {
@@ -215,8 +217,29 @@ __global__ void __launch_bounds__(kThreads)
 // is a multiple of 16 bytes; gather_kernel otherwise.  (A 16-byte vector
 // form reached 6125 GB/s on the Llama-7B layers against 6590 for this one.)
 // ---------------------------------------------------------------------------
-constexpr int kBulkChunk = 8192;
-constexpr int kBulkStages = 4;
+#ifndef ZERO_BULK_CHUNK
+#define ZERO_BULK_CHUNK 8192
+#endif
+#ifndef ZERO_BULK_STAGES
+#define ZERO_BULK_STAGES 6
+#endif
+// ZERO_GATHER_PDL=1: launch the bulk gather with programmatic dependent
+// launch, so that its CTAs become resident while the kernel before it on the
+// stream finishes and start copying the moment it has (griddepcontrol.wait).
+#ifndef ZERO_GATHER_PDL
+#define ZERO_GATHER_PDL 0
+#endif
+// ZERO_CARVEOUT >= 0: the shared-memory carveout (percent) requested for the
+// bulk gather and the consumer, so that both may share an SM in the
+// two-stream pass; -1 leaves the driver's choice.
+#ifndef ZERO_CARVEOUT
+#define ZERO_CARVEOUT -1
+#endif
+constexpr int kBulkChunk = ZERO_BULK_CHUNK;
+constexpr int kBulkStages = ZERO_BULK_STAGES;
+constexpr int kBulkRing = kBulkChunk * kBulkStages;  // dynamic shared memory per CTA
+static_assert(kBulkChunk % 16 == 0 && kBulkStages >= 2, "bulk-copy ring geometry");
+static_assert(kBulkRing <= 200 * 1024, "bulk-copy ring must fit one CTA's shared memory");
 constexpr int kBulkThreads = 32;       // one warp per CTA; lane 0 issues
 constexpr int kGatherElemBlocks = 8;   // resident blocks per SM of the element fallback
 constexpr unsigned long long kWaitNs = 2000000000ull;
@@ -251,91 +274,115 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // The pieces of one launch are numbered owner by owner: owner k's pieces of
 // all the launch's groups come before owner k+1's, so the CTAs stream one
 // rank's shard buffer at a time, as for a single group.  Within owner k,
-// group i's segment is pieces [first[i], first[i+1]).
+// group i's segment is pieces [first[i], first[i+1]).  CTA b takes pieces
+// b, b + G, b + 2G, ... (G CTAs); it walks them with a cursor (owner k, piece
+// co inside the owner, group gi holding co) instead of dividing per piece:
+// one 32-bit division where the cursor passes an owner's end, a short forward
+// scan of the group boundaries otherwise.  Piece counts stay below 2^31 (the
+// host refuses larger launches).  Each stage remembers the destination and
+// size of the piece it holds, so the store does not recompute them.
 __global__ void __launch_bounds__(kBulkThreads)
     gather_bulk_kernel(RankPtrs shards, BulkGroups bg) {
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ __align__(8) uint64_t full[kBulkStages];
+  __shared__ char* stage_dst[kBulkStages];
+  __shared__ uint32_t stage_bytes[kBulkStages];
   if (threadIdx.x != 0) return;
+#if ZERO_GATHER_PDL
+  // let the next kernel on the stream become resident now; copy only once
+  // the kernel before this one has finished and its writes are visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
   const uint32_t bar0 = smem_addr(full), buf0 = smem_addr(ring);
   for (int s = 0; s < kBulkStages; ++s)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s));
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  const int64_t G = gridDim.x, b = blockIdx.x, per_owner = bg.first[bg.ng];
-  const int64_t nchunks = per_owner * bg.n;
-  const int64_t niter = b < nchunks ? (nchunks - b + G - 1) / G : 0;
-  const int es = bg.es;
-  // piece i of this CTA: source, destination, bytes (false: outside its
-  // extent, which only the checked build can report)
-  auto piece = [&](int64_t i, const char*& src, char*& dst, uint32_t& bytes) {
-    const int64_t c = b + i * G;
-    const int k = (int)(c / per_owner);
-    const int64_t co = c - (int64_t)k * per_owner;  // piece within owner k
-    int lo = 0, hi = bg.ng - 1;  // the last group whose first piece is <= co
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (bg.first[mid] <= co) lo = mid;
-      else hi = mid - 1;
-    }
-    const int64_t S = bg.S[lo], ro = bg.rank_off[lo];
-    const int64_t off = (co - bg.first[lo]) * kBulkChunk;
+  const uint32_t G = gridDim.x, b = blockIdx.x;
+  const uint32_t per_owner = (uint32_t)bg.first[bg.ng];
+  const uint32_t nchunks = per_owner * (uint32_t)bg.n;
+  const uint32_t niter = b < nchunks ? (nchunks - b + G - 1) / G : 0;
+  const int es = bg.es, ng = bg.ng;
+  // cursor at this CTA's first piece
+  uint32_t k = b / per_owner, co = b - k * per_owner;
+  int gi = 0;
+  while (gi + 1 < ng && (uint32_t)bg.first[gi + 1] <= co) ++gi;
+
+  // issue the load of the cursor's piece into stage s, then advance
+  auto load = [&](int s) {
+    const int64_t S = bg.S[gi], ro = bg.rank_off[gi];
+    const int64_t off = (int64_t)(co - (uint32_t)bg.first[gi]) * kBulkChunk;  // bytes
     const int64_t rem = S * es - off;
-    bytes = (uint32_t)(rem < kBulkChunk ? rem : kBulkChunk);
+    const uint32_t bytes = (uint32_t)(rem < kBulkChunk ? rem : kBulkChunk);
+    const char* src = static_cast<const char*>(shards.p[k]) + ro * es + off;
+    char* dst = bg.out[gi] + (int64_t)k * S * es + off;
+    // element ranges of the checked build (compiled out of the release build)
     const int64_t so = ro + off / es, j = (int64_t)k * S + off / es, len = bytes / es;
-    src = static_cast<const char*>(shards.p[k]) + so * es;
-    dst = bg.out[lo] + j * es;
-    return in_extent(co, co + 1, bg.first[lo], bg.first[lo + 1], ZERO_SITE_GATHER_OUT) &&
-           in_extent(k, k + 1, 0, bg.n, ZERO_SITE_GATHER_SHARD) &&
-           in_extent(so, so + len, ro, ro + S, ZERO_SITE_GATHER_SHARD) &&
-           in_extent(j, j + len, 0, (int64_t)bg.n * S, ZERO_SITE_GATHER_OUT);
-  };
-  auto load = [&](int64_t i) {
-    const uint32_t bar = bar0 + 8 * (uint32_t)(i % kBulkStages);
-    const char* src;
-    char* dst;
-    uint32_t bytes;
-    if (piece(i, src, dst, bytes)) {
+    const bool ok =
+        in_extent(co, co + 1, bg.first[gi], bg.first[gi + 1], ZERO_SITE_GATHER_OUT) &&
+        in_extent(k, k + 1, 0, bg.n, ZERO_SITE_GATHER_SHARD) &&
+        in_extent(so, so + len, ro, ro + S, ZERO_SITE_GATHER_SHARD) &&
+        in_extent(j, j + len, 0, (int64_t)bg.n * S, ZERO_SITE_GATHER_OUT);
+    const uint32_t bar = bar0 + 8 * (uint32_t)s;
+    stage_dst[s] = ok ? dst : nullptr;
+    stage_bytes[s] = bytes;
+    if (ok) {
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                    "r"(bytes)
                    : "memory");
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-          "[%3];" ::"r"(buf0 + (uint32_t)(i % kBulkStages) * kBulkChunk),
+          "[%3];" ::"r"(buf0 + (uint32_t)s * kBulkChunk),
           "l"(src), "r"(bytes), "r"(bar)
           : "memory");
     } else {  // skipped piece: complete the phase with no bytes
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
     }
+    co += G;
+    if (co >= per_owner) {
+      const uint32_t q = co / per_owner;
+      k += q;
+      co -= q * per_owner;
+      gi = 0;
+    }
+    while (gi + 1 < ng && (uint32_t)bg.first[gi + 1] <= co) ++gi;
   };
-  const int64_t pro = niter < kBulkStages - 1 ? niter : kBulkStages - 1;
-  for (int64_t i = 0; i < pro; ++i) load(i);
-  int64_t loaded = pro, i = 0;
+
+  const uint32_t pro = niter < kBulkStages - 1 ? niter : kBulkStages - 1;
+  for (uint32_t i = 0; i < pro; ++i) load((int)i);
+  uint32_t loaded = pro, i = 0;
+  int s = 0;          // stage of piece i
+  uint32_t ph = 0;    // its mbarrier phase parity
   for (; i < niter; ++i) {
-    const int s = (int)(i % kBulkStages);
-    if (!mbar_wait(bar0 + 8 * s, (uint32_t)((i / kBulkStages) & 1))) {
+    if (!mbar_wait(bar0 + 8 * s, ph)) {
       atomicAdd(&g_async_timeouts, 1ull);
       break;
     }
-    const char* src;
-    char* dst;
-    uint32_t bytes;
-    if (piece(i, src, dst, bytes))
-      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                   "r"(buf0 + (uint32_t)s * kBulkChunk), "r"(bytes)
+    if (stage_dst[s])
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                       stage_dst[s]),
+                   "r"(buf0 + (uint32_t)s * kBulkChunk), "r"(stage_bytes[s])
                    : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     // refill the stage of piece i - 1 once its store has read it
-    const int64_t next = i + kBulkStages - 1;
-    if (next < niter) {
+    if (loaded < niter) {
       asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-      load(next);
-      loaded = next + 1;
+      load(s == 0 ? kBulkStages - 1 : s - 1);
+      ++loaded;
+    }
+    if (++s == kBulkStages) {
+      s = 0;
+      ph ^= 1u;
     }
   }
   // after a timeout: the loads still in flight land before the CTA exits
-  for (int64_t j = i; j < loaded; ++j)
-    if (!mbar_wait(bar0 + 8 * (int)(j % kBulkStages), (uint32_t)((j / kBulkStages) & 1)))
-      atomicAdd(&g_async_timeouts, 1ull);
+  for (uint32_t j = i; j < loaded; ++j) {
+    if (!mbar_wait(bar0 + 8 * s, ph)) atomicAdd(&g_async_timeouts, 1ull);
+    if (++s == kBulkStages) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
@@ -352,14 +399,51 @@ void bulk_add(BulkGroups& bg, int64_t S, int64_t rank_off, void* out) {
   bg.first[i + 1] = bg.first[i] + cps;
 }
 
+// The ring plus the kernel's static shared memory may pass the default 48 KiB
+// per CTA, so the kernel's dynamic limit is raised once per device.
+static cudaError_t bulk_ring_attr() {
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load() & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(gather_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kBulkRing);
+#if ZERO_CARVEOUT >= 0
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gather_bulk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             ZERO_CARVEOUT);
+#endif
+  if (e == cudaSuccess) done.fetch_or(bit);
+  return e;
+}
+
 cudaError_t launch_gather_bulk(const RankPtrs& shards, const BulkGroups& bg, int occ_kind,
                                cudaStream_t st) {
   const int64_t nchunks = bg.first[bg.ng] * bg.n;
   if (nchunks <= 0) return cudaSuccess;
+  if (nchunks >= (1ll << 31)) return cudaErrorInvalidValue;  // the kernel counts in 32 bits
+  cudaError_t e = bulk_ring_attr();
+  if (e != cudaSuccess) return e;
   int64_t grid = (int64_t)sm_count() * occupancy_cap(occ_kind);
   if (grid > nchunks) grid = nchunks;
-  gather_bulk_kernel<<<(unsigned)grid, kBulkThreads, kBulkStages * kBulkChunk, st>>>(shards, bg);
+#if ZERO_GATHER_PDL
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kBulkThreads);
+  cfg.dynamicSmemBytes = kBulkRing;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_bulk_kernel, shards, bg);
+#else
+  gather_bulk_kernel<<<(unsigned)grid, kBulkThreads, kBulkRing, st>>>(shards, bg);
   return cudaGetLastError();
+#endif
 }
 
 cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
@@ -380,6 +464,22 @@ cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& 
   else
     gather_kernel<4><<<grid, kThreads, 0, st>>>(shards, g, psi_pad, out);
   return cudaGetLastError();
+}
+
+cudaError_t launch_broadcast(const RankPtrs& shards, int elem_bytes, const GroupK& g, void* out,
+                             int occ_kind, cudaStream_t st) {
+  if (g.S <= 0) return cudaSuccess;
+  GroupK one = g;  // a group of one rank: owner k's shard alone
+  one.n = 1;
+  one.invS256 = 0.0f;
+  for (int k = 0; k < g.n; ++k) {
+    RankPtrs root{};
+    root.p[0] = shards.p[k];
+    void* dst = static_cast<char*>(out) + (int64_t)k * g.S * elem_bytes;
+    const cudaError_t e = launch_gather(root, elem_bytes, one, g.S, dst, occ_kind, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t async_timeouts(unsigned long long* out, bool reset) {
@@ -406,26 +506,45 @@ __device__ __forceinline__ unsigned long long consume_term(unsigned long long c,
   return t;
 }
 
+// c of the 8-element vector q.  (8q mod 65536) + e never wraps for e < 8, so
+// with b = 1 + (8q mod 65536), c = b * sum_e bits_e + sum_e e * bits_e: two
+// 32-bit sums (below 2^20 and 2^21) and one widening multiply.
+__device__ __forceinline__ unsigned long long vec_weighted(uint4 x, int64_t q) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t s0 = 0, s1 = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t lo = w[e] & 0xFFFFu, hi = w[e] >> 16;
+    s0 += lo + hi;
+    s1 += (uint32_t)(2 * e) * lo + (uint32_t)(2 * e + 1) * hi;
+  }
+  const uint32_t b = 1u + (((uint32_t)q & 0x1FFFu) << 3);
+  return (unsigned long long)b * s0 + s1;
+}
+
+// Vectors each thread loads before it computes: the consumer reads the layer
+// once, so bytes in flight, not arithmetic, decide its speed at one round.
+constexpr int kConsumeUnroll = 4;
+
 __global__ void __launch_bounds__(kThreads)
     checksum_kernel(const uint16_t* __restrict__ bits, int64_t n, int rounds,
                     unsigned long long* __restrict__ out) {
   unsigned long long s = 0;
-  const int64_t nv = n >> 3;
-  for (int64_t q = gtid(); q < nv; q += gstride()) {
-    if (!in_extent(q * 8, q * 8 + 8, 0, n, ZERO_SITE_CHECKSUM)) continue;
-    const uint4 x = ld_once(bits + q * 8);
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    const int64_t j0 = q * 8;
-    unsigned long long c = 0;
+  const int64_t nv = n >> 3, stride = gstride();
+  for (int64_t q0 = gtid(); q0 < nv; q0 += kConsumeUnroll * stride) {
+    uint4 x[kConsumeUnroll];
+    bool ok[kConsumeUnroll];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int64_t j = j0 + 2 * e;
-      c += (unsigned long long)(w[e] & 0xFFFFu) * (1ull + (unsigned long long)(j & 0xFFFF));
-      c += (unsigned long long)(w[e] >> 16) * (1ull + (unsigned long long)((j + 1) & 0xFFFF));
+    for (int u = 0; u < kConsumeUnroll; ++u) {
+      const int64_t q = q0 + u * stride;
+      ok[u] = q < nv && in_extent(q * 8, q * 8 + 8, 0, n, ZERO_SITE_CHECKSUM);
+      if (ok[u]) x[u] = ld_once(bits + q * 8);
     }
-    s += consume_term(c, rounds);
+#pragma unroll
+    for (int u = 0; u < kConsumeUnroll; ++u)
+      if (ok[u]) s += consume_term(vec_weighted(x[u], q0 + u * stride), rounds);
   }
-  for (int64_t j = (nv << 3) + gtid(); j < n; j += gstride())
+  for (int64_t j = (nv << 3) + gtid(); j < n; j += stride)
     if (in_extent(j, j + 1, 0, n, ZERO_SITE_CHECKSUM))
       s += consume_term((unsigned long long)bits[j] * (1ull + (unsigned long long)(j & 0xFFFF)),
                         rounds);
@@ -435,13 +554,31 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 cudaError_t launch_checksum(const void* layer, int64_t n, int rounds, uint64_t* out,
-                            cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(uint64_t), st);
-  if (e != cudaSuccess) return e;
+                            cudaStream_t st, bool clear) {
+  if (clear) {
+    const cudaError_t e = cudaMemsetAsync(out, 0, sizeof(uint64_t), st);
+    if (e != cudaSuccess) return e;
+  }
   if (n <= 0) return cudaSuccess;
-  checksum_kernel<<<(unsigned)wave_grid(checksum_kernel, n / 8 + 1, ZERO_OCC_CONSUMER), kThreads,
-                    0, st>>>(static_cast<const uint16_t*>(layer), n, rounds,
-                             reinterpret_cast<unsigned long long*>(out));
+#if ZERO_CARVEOUT >= 0
+  {
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(done.load() & bit)) {
+      e = cudaFuncSetAttribute(checksum_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               ZERO_CARVEOUT);
+      if (e != cudaSuccess) return e;
+      done.fetch_or(bit);
+    }
+  }
+#endif
+  const int64_t items = (n / 8) / kConsumeUnroll + 1;
+  checksum_kernel<<<(unsigned)wave_grid(checksum_kernel, items, ZERO_OCC_CONSUMER), kThreads, 0,
+                    st>>>(static_cast<const uint16_t*>(layer), n, rounds,
+                          reinterpret_cast<unsigned long long*>(out));
   return cudaGetLastError();
 }
 

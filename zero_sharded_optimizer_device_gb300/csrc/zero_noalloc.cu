@@ -15,12 +15,15 @@
 // Host code cannot use the array's name as a device address, so the first
 // call on each device looks the address up with cudaGetSymbolAddress (with
 // that device current) and caches it; that first call should come before
-// any stream capture.  Every call reuses the same slots: a call writes the
-// first zero_rs_partials() slots (every block of its reduce-scatter writes
-// its own slot, blocks without work write 0) before the norm kernel reads
-// exactly those slots, so nothing has to be cleared between calls, but two
-// calls that overlap on the GPU (different streams, no ordering between
-// them) race on the slots and may both return a wrong norm.
+// any stream capture.  Every call reuses the same slots: a call fixes its
+// reduce-scatter grid once, every block of that launch writes its own slot
+// (blocks without work write 0), and the norm kernel then reads exactly those
+// slots, so nothing has to be cleared between calls, and a zero_set_occupancy
+// on another host thread cannot change the grid between the launch and the
+// norm.  An empty window launches no reduce-scatter and reads no slot (norm
+// 0, coefficient 1).  Two calls that overlap on the GPU (different streams,
+// no ordering between them) race on the slots and may both return a wrong
+// norm.
 #include <math.h>
 
 #include <mutex>
@@ -71,9 +74,8 @@ extern "C" int zero_reduce_scatter_norm_static(const zero_plan_t* plan, int32_t 
   if ((d_norm && !aligned4(d_norm)) || (d_coef && !aligned4(d_coef))) return ZERO_EALIGN;
   if (!(gdtype == ZERO_F32 || gdtype == ZERO_BF16)) return ZERO_EDTYPE;
   if (begin < 0 || end < begin) return ZERO_ERANGE;
-  int64_t n = 0;
-  int s = zero_rs_partials(plan, gdtype, end - begin, &n);
-  if (s != ZERO_OK) return s;
+  // the grid, and with it the number of slots written and read, is fixed here
+  const int64_t n = end > begin ? zk::rs_partials_for(plan->n_ranks, gdtype, end - begin) : 0;
   if (n > kStaticPartials) return ZERO_ERANGE;  // more partials than static slots
   double* partials = nullptr;
   const int ce = static_partials(&partials);
@@ -81,8 +83,8 @@ extern "C" int zero_reduce_scatter_norm_static(const zero_plan_t* plan, int32_t 
     zk::record_cuda_error(ce);
     return ZERO_ECUDA;
   }
-  s = zero_reduce_scatter(plan, group, grads, gdtype, reduced, begin, end, grad_scale, partials,
-                          stream);
+  int s = zk::reduce_scatter_entry(plan, group, grads, gdtype, reduced, begin, end, grad_scale,
+                                   partials, n, (cudaStream_t)stream);
   if (s != ZERO_OK) return s;
   return zero_grad_norm(partials, n, max_norm, d_norm, d_coef, stream);
 }

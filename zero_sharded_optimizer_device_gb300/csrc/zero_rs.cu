@@ -40,8 +40,8 @@ int64_t grid_for(int64_t items, int threads, int per_sm) {
 // Occupancy caps (resident 256-thread blocks per SM) of the kernel families.
 // Measured on GB300 with the benchmark's workloads: HBM throughput of these
 // streaming kernels often peaks below full occupancy, because fewer
-// concurrent request streams per SM keep DRAM accesses more local; see the
-// design notes for the sweep.  zero_set_occupancy() overrides them.
+// concurrent request streams per SM keep DRAM accesses more local (the sweep
+// below).  zero_set_occupancy() overrides them.
 namespace {
 // Best caps of a sweep on GB300 with the workloads' random data (GB/s):
 // fused N=8 step 3 (6699; 6326 at 2, 6097 at 4), fused N=16 3 (7069), Adam
@@ -340,8 +340,9 @@ struct RsLaunch {
   }
   static cudaError_t run(const RankPtrs& src, const GroupK& g, int64_t begin, int64_t end,
                          float* reduced, float scale, double* partials, int mode,
-                         cudaStream_t st) {
-    rs_kernel<NT, GT><<<(unsigned)grid(end - begin), kThreads, 0, st>>>(
+                         cudaStream_t st, int64_t fixed) {
+    const int64_t blocks = fixed > 0 ? fixed : grid(end - begin);
+    rs_kernel<NT, GT><<<(unsigned)blocks, kThreads, 0, st>>>(
         src, g, begin, end, reduced, scale, partials, mode);
     return cudaGetLastError();
   }
@@ -383,10 +384,10 @@ int64_t rs_partials_for(int n, int gdtype, int64_t n_elements) {
 
 cudaError_t launch_reduce_scatter(const RankPtrs& src, int gdtype, const GroupK& g,
                                   float* reduced, int64_t begin, int64_t end, float scale,
-                                  double* partials, int mode, cudaStream_t st) {
+                                  double* partials, int mode, cudaStream_t st, int64_t grid) {
   if (end <= begin) return cudaSuccess;
   return dispatch<RsLaunch>(g.n, gdtype, src, g, begin, end, reduced, scale, partials, mode,
-                            st);
+                            st, grid);
 }
 
 cudaError_t launch_fused(const RankPtrs& src, int gdtype, const GroupK& g, int64_t begin,

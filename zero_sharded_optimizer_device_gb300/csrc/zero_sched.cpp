@@ -124,11 +124,14 @@ static int gather_pass(const zero_plan_t* plan, const int32_t* first, const int3
   if (e == cudaSuccess) e = cudaEventRecord(ev.e[0], sa);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(sb, ev.e[0], 0);
   if (e == cudaSuccess) e = issue(0);
+  // every consumer's sum zeroed at once, off the per-layer path
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_sums, 0, sizeof(uint64_t) * (size_t)n, sa);
   for (int32_t j = 0; j < n && e == cudaSuccess; ++j) {
     if (j + 1 < n) e = issue(j + 1);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(sa, ev.e[1 + (j & 1)], 0);
     if (e == cudaSuccess)
-      e = zk::launch_checksum(layer_bufs[j & 1], step_elems[j], consumer_rounds, d_sums + j, sa);
+      e = zk::launch_checksum(layer_bufs[j & 1], step_elems[j], consumer_rounds, d_sums + j, sa,
+                              false);
     if (e == cudaSuccess) e = cudaEventRecord(ev.e[3 + (j & 1)], sa);
   }
   nvtxRangePop();
