@@ -208,38 +208,30 @@ __global__ void __launch_bounds__(kThreads)
 // Stage-3 gather with 1-D bulk copies (TMA).  The layer is N contiguous
 // segments (owner k's S elements land at k*S), cut into pieces of up to
 // kBulkChunk bytes.  One thread per CTA moves its pieces global -> shared ->
-// global through a ring of kBulkStages buffers: a piece's load completes on
-// its stage's mbarrier (expect_tx), its store is a bulk-group copy, and a
-// stage is refilled once the store that read it has finished reading.  Every
-// mbarrier wait gives up after ~2 s: the timeout is counted in
-// g_async_timeouts (zero_async_status), the CTA lets the loads it issued
-// land (again bounded) and returns.  Used when every segment start and length
-// is a multiple of 16 bytes; gather_kernel otherwise.  (A 16-byte vector
-// form reached 6125 GB/s on the Llama-7B layers against 6590 for this one.)
+// global through a ring of STAGES buffers: a piece's load completes on its
+// stage's mbarrier (expect_tx), its store is a bulk-group copy, and a stage is
+// refilled once the store that read it has finished reading.  Every mbarrier
+// wait gives up after ~2 s: the timeout is counted in g_async_timeouts
+// (zero_async_status), the CTA lets the loads it issued land (again bounded)
+// and returns.  Used when every segment start and length is a multiple of 16
+// bytes; gather_kernel otherwise.
+//
+// Ring depth and launch, measured over the 68 Llama-7B gathers (GB/s at 1 /
+// 2 / 3 / 4 CTAs per SM): 8 KiB x 4 stages 5234 / 6619 / 6201 / 6294, x 6
+// stages 6158 / 6237 / 6175 / 6136; 16 KiB x 4 6437 / 6287 / 6135 / 6256;
+// 32 KiB x 3 6614 / 6299 / 6369 / 6416 -- about 48-64 KiB of loads in flight
+// per SM is best, more is slower.  Inside the two-stream pass, beside the
+// consumer, the deeper ring is better (pass 12.3 ms at 6 stages against 13.0
+// at 4, 2 CTAs per SM beside 7 consumer blocks).  Standalone gathers also use
+// programmatic dependent launch (PDL): the CTAs become resident while the
+// kernel before them finishes and start copying once it has
+// (griddepcontrol.wait), which removes the gap between back-to-back gathers
+// (68 gathers +1.4 %, the 16 launches of a broadcast -11 % time); inside the
+// pass the gathers wait on events anyway, and PDL there measured 1.6 % slower.
 // ---------------------------------------------------------------------------
-#ifndef ZERO_BULK_CHUNK
-#define ZERO_BULK_CHUNK 8192
-#endif
-#ifndef ZERO_BULK_STAGES
-#define ZERO_BULK_STAGES 6
-#endif
-// ZERO_GATHER_PDL=1: launch the bulk gather with programmatic dependent
-// launch, so that its CTAs become resident while the kernel before it on the
-// stream finishes and start copying the moment it has (griddepcontrol.wait).
-#ifndef ZERO_GATHER_PDL
-#define ZERO_GATHER_PDL 0
-#endif
-// ZERO_CARVEOUT >= 0: the shared-memory carveout (percent) requested for the
-// bulk gather and the consumer, so that both may share an SM in the
-// two-stream pass; -1 leaves the driver's choice.
-#ifndef ZERO_CARVEOUT
-#define ZERO_CARVEOUT -1
-#endif
-constexpr int kBulkChunk = ZERO_BULK_CHUNK;
-constexpr int kBulkStages = ZERO_BULK_STAGES;
-constexpr int kBulkRing = kBulkChunk * kBulkStages;  // dynamic shared memory per CTA
-static_assert(kBulkChunk % 16 == 0 && kBulkStages >= 2, "bulk-copy ring geometry");
-static_assert(kBulkRing <= 200 * 1024, "bulk-copy ring must fit one CTA's shared memory");
+constexpr int kBulkChunk = 8192;
+constexpr int kBulkStagesAlone = 4;     // zero_gather_layer, zero_gather_groups, broadcast
+constexpr int kBulkStagesPrefetch = 6;  // inside zero_stage3_gather_pass
 constexpr int kBulkThreads = 32;       // one warp per CTA; lane 0 issues
 constexpr int kGatherElemBlocks = 8;   // resident blocks per SM of the element fallback
 constexpr unsigned long long kWaitNs = 2000000000ull;
@@ -281,21 +273,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // scan of the group boundaries otherwise.  Piece counts stay below 2^31 (the
 // host refuses larger launches).  Each stage remembers the destination and
 // size of the piece it holds, so the store does not recompute them.
+template <int STAGES, bool PDL>
 __global__ void __launch_bounds__(kBulkThreads)
     gather_bulk_kernel(RankPtrs shards, BulkGroups bg) {
   extern __shared__ __align__(128) unsigned char ring[];
-  __shared__ __align__(8) uint64_t full[kBulkStages];
-  __shared__ char* stage_dst[kBulkStages];
-  __shared__ uint32_t stage_bytes[kBulkStages];
+  __shared__ __align__(8) uint64_t full[STAGES];
+  __shared__ char* stage_dst[STAGES];
+  __shared__ uint32_t stage_bytes[STAGES];
   if (threadIdx.x != 0) return;
-#if ZERO_GATHER_PDL
-  // let the next kernel on the stream become resident now; copy only once
-  // the kernel before this one has finished and its writes are visible
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-#endif
+  if constexpr (PDL) {
+    // let the next kernel on the stream become resident now; copy only once
+    // the kernel before this one has finished and its writes are visible
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
   const uint32_t bar0 = smem_addr(full), buf0 = smem_addr(ring);
-  for (int s = 0; s < kBulkStages; ++s)
+  for (int s = 0; s < STAGES; ++s)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s));
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   const uint32_t G = gridDim.x, b = blockIdx.x;
@@ -348,7 +341,7 @@ __global__ void __launch_bounds__(kBulkThreads)
     while (gi + 1 < ng && (uint32_t)bg.first[gi + 1] <= co) ++gi;
   };
 
-  const uint32_t pro = niter < kBulkStages - 1 ? niter : kBulkStages - 1;
+  const uint32_t pro = niter < STAGES - 1 ? niter : STAGES - 1;
   for (uint32_t i = 0; i < pro; ++i) load((int)i);
   uint32_t loaded = pro, i = 0;
   int s = 0;          // stage of piece i
@@ -367,10 +360,10 @@ __global__ void __launch_bounds__(kBulkThreads)
     // refill the stage of piece i - 1 once its store has read it
     if (loaded < niter) {
       asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-      load(s == 0 ? kBulkStages - 1 : s - 1);
+      load(s == 0 ? STAGES - 1 : s - 1);
       ++loaded;
     }
-    if (++s == kBulkStages) {
+    if (++s == STAGES) {
       s = 0;
       ph ^= 1u;
     }
@@ -378,7 +371,7 @@ __global__ void __launch_bounds__(kBulkThreads)
   // after a timeout: the loads still in flight land before the CTA exits
   for (uint32_t j = i; j < loaded; ++j) {
     if (!mbar_wait(bar0 + 8 * s, ph)) atomicAdd(&g_async_timeouts, 1ull);
-    if (++s == kBulkStages) {
+    if (++s == STAGES) {
       s = 0;
       ph ^= 1u;
     }
@@ -401,6 +394,7 @@ void bulk_add(BulkGroups& bg, int64_t S, int64_t rank_off, void* out) {
 
 // The ring plus the kernel's static shared memory may pass the default 48 KiB
 // per CTA, so the kernel's dynamic limit is raised once per device.
+template <int STAGES, bool PDL>
 static cudaError_t bulk_ring_attr() {
   static std::atomic<unsigned long long> done{0};
   int dev = 0;
@@ -408,15 +402,28 @@ static cudaError_t bulk_ring_attr() {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (done.load() & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(gather_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kBulkRing);
-#if ZERO_CARVEOUT >= 0
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gather_bulk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             ZERO_CARVEOUT);
-#endif
+  e = cudaFuncSetAttribute(gather_bulk_kernel<STAGES, PDL>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, STAGES * kBulkChunk);
   if (e == cudaSuccess) done.fetch_or(bit);
   return e;
+}
+
+template <int STAGES, bool PDL>
+static cudaError_t launch_bulk(const RankPtrs& shards, const BulkGroups& bg, int64_t grid,
+                               cudaStream_t st) {
+  cudaError_t e = bulk_ring_attr<STAGES, PDL>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kBulkThreads);
+  cfg.dynamicSmemBytes = STAGES * kBulkChunk;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gather_bulk_kernel<STAGES, PDL>, shards, bg);
 }
 
 cudaError_t launch_gather_bulk(const RankPtrs& shards, const BulkGroups& bg, int occ_kind,
@@ -424,26 +431,11 @@ cudaError_t launch_gather_bulk(const RankPtrs& shards, const BulkGroups& bg, int
   const int64_t nchunks = bg.first[bg.ng] * bg.n;
   if (nchunks <= 0) return cudaSuccess;
   if (nchunks >= (1ll << 31)) return cudaErrorInvalidValue;  // the kernel counts in 32 bits
-  cudaError_t e = bulk_ring_attr();
-  if (e != cudaSuccess) return e;
   int64_t grid = (int64_t)sm_count() * occupancy_cap(occ_kind);
   if (grid > nchunks) grid = nchunks;
-#if ZERO_GATHER_PDL
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kBulkThreads);
-  cfg.dynamicSmemBytes = kBulkRing;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gather_bulk_kernel, shards, bg);
-#else
-  gather_bulk_kernel<<<(unsigned)grid, kBulkThreads, kBulkRing, st>>>(shards, bg);
-  return cudaGetLastError();
-#endif
+  if (occ_kind == ZERO_OCC_PREFETCH)
+    return launch_bulk<kBulkStagesPrefetch, false>(shards, bg, grid, st);
+  return launch_bulk<kBulkStagesAlone, true>(shards, bg, grid, st);
 }
 
 cudaError_t launch_gather(const RankPtrs& shards, int elem_bytes, const GroupK& g,
@@ -560,21 +552,6 @@ cudaError_t launch_checksum(const void* layer, int64_t n, int rounds, uint64_t* 
     if (e != cudaSuccess) return e;
   }
   if (n <= 0) return cudaSuccess;
-#if ZERO_CARVEOUT >= 0
-  {
-    static std::atomic<unsigned long long> done{0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(done.load() & bit)) {
-      e = cudaFuncSetAttribute(checksum_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               ZERO_CARVEOUT);
-      if (e != cudaSuccess) return e;
-      done.fetch_or(bit);
-    }
-  }
-#endif
   const int64_t items = (n / 8) / kConsumeUnroll + 1;
   checksum_kernel<<<(unsigned)wave_grid(checksum_kernel, items, ZERO_OCC_CONSUMER), kThreads, 0,
                     st>>>(static_cast<const uint16_t*>(layer), n, rounds,
