@@ -77,6 +77,11 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def local_ranks() -> int:
+    """Ranks on this host (each pins its own end-to-end buffers)."""
+    return max(1, int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
+
+
 # ----------------------------------------------------------------- clocks --
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
@@ -400,12 +405,13 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
     # reported with its mode.
     host_bytes = N * P * gbytes + P * 2
     ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
-    if host_bytes > 0.4 * ram:      # too large to pin on this host: no end-to-end leg
+    if host_bytes * local_ranks() > 0.4 * ram:  # too large to pin on this host: no e2e leg
         return dict(local_ms=local_ms, launch_ms=launch_ms, e2e_ms=None, psi=w.psi, psi_pad=P,
                     n_ranks=N, gbytes=gbytes, copy_gbs=copy_gbs, clocks=clocks.summary(),
                     h2d=N * P * gbytes, d2h=P * 2, e2e_steps=0,
                     e2e_transfer=f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
-                                 f"exceeds 40% of the host's {ram / 1e9:.0f} GB")
+                                 f"x {local_ranks()} local ranks exceeds 40% of the host's "
+                                 f"{ram / 1e9:.0f} GB")
     pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
     h_grads = [pinned[r * P * gbytes:(r + 1) * P * gbytes].view(gdt) for r in range(N)]
     for r in range(N):
@@ -455,19 +461,17 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
 
 
 # ----------------------------------------- bucketed pipeline with clipping --
-def _timed_launches(stream, calls):
-    """Run callables on `stream`, each bracketed by CUDA events; returns the
-    per-call device milliseconds (after a synchronize)."""
+def _timed_seq(stream, f) -> float:
+    """Device milliseconds of everything f enqueues on `stream` (one event
+    pair around the whole sequence, so back-to-back launches stay back to
+    back)."""
     import torch
-    evs = []
-    for f in calls:
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        f()
-        b.record(stream)
-        evs.append((a, b))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    f()
+    b.record(stream)
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in evs]
+    return a.elapsed_time(b)
 
 
 def bench_bucketed(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = False) -> dict:
@@ -553,9 +557,10 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = F
     if kernel_only:
         return res
     ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
-    if host_bytes > 0.4 * ram:
+    if host_bytes * local_ranks() > 0.4 * ram:
         res["e2e_transfer"] = (f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
-                               f"exceeds 40% of the host's {ram / 1e9:.0f} GB")
+                               f"x {local_ranks()} local ranks exceeds 40% of the host's "
+                               f"{ram / 1e9:.0f} GB")
         return res
     pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
     h_grads = [pinned[r * P * gb:(r + 1) * P * gb].view(gdt) for r in range(N)]
@@ -718,12 +723,7 @@ def _stage3_gathers(Z, plan, groups, shards, dev, sa, steps, use_graph) -> dict:
     order = list(range(G)) + list(reversed(range(G)))
 
     def timed(f):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(sa)
-        f()
-        e1.record(sa)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
+        return _timed_seq(sa, f)
 
     def schedule(rounds):
         return lambda: Z.zero_stage3_gather_pass(plan, order, shards, bufs, gmax, sums, rounds,
@@ -781,9 +781,10 @@ def _stage3_e2e(Z, plan, groups, N, ST, slot, master, m, v, sa, t) -> dict:
     host_bytes = N * gmax * 2 + N * ST * 2
     ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
     base = dict(e2e_ms=None, h2d=h2d, d2h=d2h, e2e_steps=0)
-    if host_bytes > 0.4 * ram:
+    if host_bytes * local_ranks() > 0.4 * ram:
         return dict(base, e2e_transfer=f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
-                                       f"exceeds 40% of the host's {ram / 1e9:.0f} GB")
+                                       f"x {local_ranks()} local ranks exceeds 40% of the "
+                                       f"host's {ram / 1e9:.0f} GB")
     pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
     h_slot = [pinned[r * gmax * 2:(r + 1) * gmax * 2].view(torch.bfloat16) for r in range(N)]
     off = N * gmax * 2
@@ -895,8 +896,12 @@ def bench_gather_sweep(w, steps: int, dist: Dist, only=None) -> dict:
             calls = [lambda j=j, gi=gi: Z.zero_gather_layer(plan, gi, shards, Z.ZERO_BF16,
                                                             bufs[j % 2], sa)
                      for j, gi in enumerate(order)]
-        _timed_launches(sa, calls)                     # warm-up
-        ms = statistics.fmean(sum(_timed_launches(sa, calls)) for _ in range(steps))
+        def run_all():
+            for f in calls:
+                f()
+
+        _timed_seq(sa, run_all)                          # warm-up
+        ms = statistics.fmean(_timed_seq(sa, run_all) for _ in range(steps))
         elems = 2 * sum(g["psi_pad"] for g in groups)
         res[per] = {"groups": len(groups), "gathers": len(order), "ms": ms,
                     "gbs": 4 * elems / (ms * 1e-3) / 1e9,
