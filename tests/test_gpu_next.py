@@ -712,3 +712,64 @@ def test_prepared_step_equals_zero_step(cuda):
         assert_bf16(bits_of(out), r["full"], "gathered")
         outs.append((c.master.clone(), out.clone()))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_gathers_queued_right_after_the_step_that_writes_their_shards(cuda):
+    """The standalone bulk gather uses programmatic dependent launch: its CTAs
+    may become resident before the kernel ahead of it on the stream has
+    finished, and they copy only after griddepcontrol.wait.  Here each
+    group's fused step writes the owners' shards and the group's gather, then
+    its broadcast form, are queued right behind it with no synchronisation
+    in between; every layer equals the oracle's gather of the owners' bf16
+    shards, cast from the oracle's updated master."""
+    import torch
+    d, ffn, vocab = 64, 172, 500
+    blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(3)]
+    numels = [vocab * d] + [n for b in blocks for n in b] + [d, vocab * d]
+    groups = [0] + [1 + i // 9 for i in range(27)] + [4, 4]
+    c = Case(numels, 16, 16, "bf16", seed=23, groups=groups)
+    Z = c.Z
+    N, G = 16, len(c.groups)
+    shards = [torch.full((c.info["shard_total"],), 7.0, dtype=torch.bfloat16, device=cuda)
+              for _ in range(N)]
+    lay_a = [torch.zeros(g["psi_pad"], dtype=torch.bfloat16, device=cuda) for g in c.groups]
+    lay_b = [torch.zeros(g["psi_pad"], dtype=torch.bfloat16, device=cuda) for g in c.groups]
+    grads = [c.grads_dev(gi, 1) for gi in range(G)]
+    torch.cuda.synchronize()
+    for gi in reversed(range(G)):
+        Z.zero_step_group(c.plan, gi, grads[gi], Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(1),
+                          None, shards)
+        Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, lay_a[gi])
+        Z.zero_broadcast_layer(c.plan, gi, shards, Z.ZERO_BF16, lay_b[gi])
+    torch.cuda.synchronize()
+    for gi in reversed(range(G)):
+        c.oracle_step(gi, 1)
+    c.check_state("stage 3, gathers queued behind the step")
+    for gi, g in enumerate(c.groups):
+        f0, S = g["flat_off"], g["shard"]
+        own = [O.f32_to_bf16(c.h_master[f0 + k * S:f0 + (k + 1) * S]) for k in range(N)]
+        want, _, _ = O.gather_layer(own)
+        want_b, _, _, _ = O.broadcast_gather(own)
+        assert np.array_equal(bits_of(lay_a[gi]), want), gi
+        assert np.array_equal(bits_of(lay_b[gi]), want_b), gi
+    # the same gathers captured once in a CUDA graph (programmatic launches
+    # become graph edges) and replayed into cleared buffers
+    for t in lay_a + lay_b:
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s), torch.cuda.graph(g, stream=s):
+        for gi in range(G):
+            Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, lay_a[gi], s)
+            Z.zero_broadcast_layer(c.plan, gi, shards, Z.ZERO_BF16, lay_b[gi], s)
+    torch.cuda.current_stream().wait_stream(s)
+    for t in lay_a + lay_b:
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for gi, gg in enumerate(c.groups):
+        f0, S = gg["flat_off"], gg["shard"]
+        own = [O.f32_to_bf16(c.h_master[f0 + k * S:f0 + (k + 1) * S]) for k in range(N)]
+        assert np.array_equal(bits_of(lay_a[gi]), O.gather_layer(own)[0]), ("graph", gi)
+        assert np.array_equal(bits_of(lay_b[gi]), O.broadcast_gather(own)[0]), ("graph", gi)

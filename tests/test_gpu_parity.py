@@ -275,6 +275,15 @@ def test_empty_plan_and_empty_window_are_noops(cuda):
     x = torch.zeros(16, device=cuda)
     grads = [torch.zeros(16, device=cuda) for _ in range(4)]
     Z.zero_step(p, 0, grads, Z.ZERO_F32, x, x, x, Z.adam_hp(1, 0.25), None, None)
+    # an empty stage-3 group (its tensors have no elements): gathers write nothing
+    pe = Z.zero_plan([64, 0, 64], 4, 16, [0, 1, 2])
+    assert Z.zero_plan_group(pe, 1)["psi_pad"] == 0
+    sh = [torch.zeros(64, dtype=torch.bfloat16, device=cuda) for _ in range(4)]
+    canary = torch.full((16,), 3.0, dtype=torch.bfloat16, device=cuda)
+    Z.zero_gather_layer(pe, 1, sh, Z.ZERO_BF16, canary)
+    Z.zero_broadcast_layer(pe, 1, sh, Z.ZERO_BF16, canary)
+    torch.cuda.synchronize()
+    assert bool((canary == 3.0).all())
     c = Case([100], 4, 1, "f32", seed=3)
     before = c.master.clone()
     red = torch.full((c.info["psi_pad"],), 7.0, device=cuda)

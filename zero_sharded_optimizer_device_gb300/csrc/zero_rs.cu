@@ -46,14 +46,15 @@ namespace {
 // Best caps of a sweep on GB300 with the workloads' random data (GB/s):
 // fused N=8 step 3 (6699; 6326 at 2, 6097 at 4), fused N=16 3 (7069), Adam
 // 2 (6418; 5775 at 4), reduce-scatter with norm partials 8 (6550-6732;
-// 5780 at 3), stage-3 gather 8 (6522; 4444 at 3), all-gather cast 4 (6494).
-// The stage-3 gather's bulk-copy form (one issuing thread per CTA, 4 x 8 KiB
-// ring) over the 68 Llama-7B gathers: 2 CTAs per SM 6590 (6300 at 4; the
-// 16-byte vector form peaks at 6125 with 8 blocks per SM).  Two-stream
-// gather pass (ms, 68 gathers + consumers): the gathers and the consumer
-// must fit on an SM together to overlap at all; bulk gathers at 2 CTAs
-// beside a 7-block consumer gave 12.8 (one-round consumer) and 32.1
-// (64 rounds), against 12.5 and 34.2 for vector gathers at 4 + 4 blocks.
+// 5780 at 3), all-gather cast 4 (6494).  The stage-3 gather's bulk-copy form
+// (one issuing thread per CTA, 4 x 8 KiB ring) over the 68 Llama-7B gathers:
+// 2 CTAs per SM 6619-6758 (5234 at 1, 6201 at 3, 6294 at 4; the retired
+// 16-byte vector form peaked at 6125 with 8 blocks per SM).  Two-stream
+// gather pass (ms, 68 gathers + consumers; prefetch CTAs x consumer blocks
+// per SM): the two kernels must fit on an SM together to overlap at all;
+// 2 x 7 gave 12.28 (one-round consumer) and 28.12 (64 rounds), 4 x 4 11.89
+// and 30.55, 3 x 6 12.23 and 29.11, 2 x 5 12.30 and 28.68: the default
+// favours the arithmetic-bound consumer, whose time prefetch exists to hide.
 constexpr int kOccDefault[ZERO_OCC_KINDS] = {
     3,   // ZERO_OCC_FUSED
     8,   // ZERO_OCC_RS
