@@ -318,7 +318,11 @@ int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* g
  * S_g and rank_off(g) are multiples of 16 bytes the N segments move by 1-D
  * bulk copies (TMA) through shared memory, issued by one thread per CTA;
  * their waits are bounded (see zero_async_status).  Otherwise element by
- * element. */
+ * element.  The bulk-copy kernel is launched with programmatic dependent
+ * launch: its CTAs may become resident while the kernel before it on the
+ * stream is still running, but they copy only after that kernel has finished
+ * and its writes are visible, so stream order holds as for any launch (also
+ * inside a captured CUDA graph). */
 int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
                       zero_dtype_t dtype, void* layer_out, zero_stream_t stream);
 
@@ -370,8 +374,10 @@ int zero_gather_groups(const zero_plan_t* plan, const int32_t* groups, int32_t k
  * d_sums: n uint64.  1 <= consumer_rounds <= ZERO_MAX_CONSUMER_ROUNDS.
  * The two kernels overlap only if their blocks fit on an SM together: the
  * gathers launch at the ZERO_OCC_PREFETCH cap and the consumer at the
- * ZERO_OCC_CONSUMER cap (by default 2 one-warp bulk-copy CTAs beside 7 of
- * the 8 resident 256-thread blocks; see zero_set_occupancy).
+ * ZERO_OCC_CONSUMER cap (by default 2 one-warp bulk-copy CTAs with a 6-stage
+ * ring beside the consumer's cap of 7 256-thread blocks, of which its
+ * register use lets 6 be resident; see zero_set_occupancy).  The call zeroes
+ * d_sums[0..n) on stream_a before the first consumer.
  * stream_a != stream_b.  Uses five CUDA events created
  * and released inside the call; allocates no device memory.  The call may be
  * captured in a CUDA graph: with stream_a capturing, stream_b joins the

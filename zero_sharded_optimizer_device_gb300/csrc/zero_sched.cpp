@@ -8,9 +8,10 @@
 // one of two layer buffers while stream A consumes the current one.  The two
 // kernels can only run at the same time if their blocks fit on an SM
 // together, so the gathers launch with their own occupancy cap
-// (ZERO_OCC_PREFETCH, default 2 one-warp bulk-copy CTAs per SM) beside the
-// consumer's (ZERO_OCC_CONSUMER, default 7 of the 8 resident 256-thread
-// blocks).
+// (ZERO_OCC_PREFETCH, default 2 one-warp bulk-copy CTAs per SM, each with a
+// 6-stage ring) beside the consumer's (ZERO_OCC_CONSUMER, default 7
+// 256-thread blocks, of which the consumer's register use lets 6 be
+// resident).
 #include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
