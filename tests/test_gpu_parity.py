@@ -621,6 +621,47 @@ def test_zero_copy_host_buffers_match_device_buffers(cuda):
     assert torch.equal(h_out, out.cpu())
 
 
+def test_zero_copy_stage3_slot_and_shards_match_device_buffers(cuda):
+    """The end-to-end form of the stage-3 step: every group's N gradient
+    buffers are prefixes of one mapped page-locked host slot, and the owners'
+    bf16 shards are written to mapped host buffers over the link.  The state
+    and shards equal, bit for bit, those of the same step from device
+    buffers, and the oracle's."""
+    import torch
+    import bench
+    w = W.mini(W.LLAMA_7B_STAGE3, scale=4096)
+    c = Case(w.numels, w.n_ranks, w.align, w.grad_dtype, w.grad_sigma, w.master_sigma, w.seed,
+             groups=w.groups)
+    Z = c.Z
+    N, G, ST = c.n, len(c.groups), c.info["shard_total"]
+    gmax = max(g["psi_pad"] for g in c.groups)
+    h_slot = [torch.zeros(gmax, dtype=torch.bfloat16, pin_memory=True) for _ in range(N)]
+    h_shards = [torch.zeros(ST, dtype=torch.bfloat16, pin_memory=True) for _ in range(N)]
+    if not all(bench.host_mapped(x) for x in h_slot + h_shards):
+        pytest.skip("pinned host memory is not mapped into the device address space")
+    d_slot = [torch.zeros(gmax, dtype=torch.bfloat16, device=cuda) for _ in range(N)]
+    d_shards = [torch.zeros(ST, dtype=torch.bfloat16, device=cuda) for _ in range(N)]
+    master2, m2, v2 = c.master.clone(), c.m.clone(), c.v.clone()
+    for gi in reversed(range(G)):
+        g = c.groups[gi]
+        views = [t[:g["psi_pad"]] for t in d_slot]
+        c.grads_dev(gi, 1, views)
+        torch.cuda.synchronize()
+        for h, d in zip(h_slot, d_slot):
+            h.copy_(d)
+        h_views = [t[:g["psi_pad"]] for t in h_slot]
+        Z.zero_step_group(c.plan, gi, views, Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(1), None,
+                          d_shards)
+        Z.zero_step_group(c.plan, gi, h_views, Z.ZERO_BF16, master2, m2, v2, c.hp_dev(1), None,
+                          h_shards)
+        torch.cuda.synchronize()
+        c.oracle_step(gi, 1)
+    assert torch.equal(master2, c.master) and torch.equal(m2, c.m) and torch.equal(v2, c.v)
+    for h, d in zip(h_shards, d_shards):
+        assert torch.equal(h, d.cpu())
+    c.check_state("stage 3 from host buffers")
+
+
 def test_large_step_numbers(cuda):
     """Step numbers where 1 - beta^t has reached 1 in fp32 (and beta1^t has
     underflowed): the bias corrections agree with the oracle's."""
