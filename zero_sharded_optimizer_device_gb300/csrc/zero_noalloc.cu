@@ -25,6 +25,7 @@
 // no ordering between them) race on the slots and may both return a wrong
 // norm.
 #include <math.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <mutex>
 
@@ -68,6 +69,10 @@ extern "C" int zero_reduce_scatter_norm_static(const zero_plan_t* plan, int32_t 
                                                float* reduced, int64_t begin, int64_t end,
                                                float grad_scale, float max_norm, float* d_norm,
                                                float* d_coef, zero_stream_t stream) {
+  struct Range {  // NVTX range around the call, as for every device entry point
+    Range() { nvtxRangePushA("zero_reduce_scatter_norm_static"); }
+    ~Range() { nvtxRangePop(); }
+  } nvtx;
   // checks of the norm's own arguments first, so that a rejected call
   // launches nothing; zero_reduce_scatter checks the rest
   if (!plan || !isfinite(max_norm) || !(max_norm > 0.0f)) return ZERO_EINVAL;
