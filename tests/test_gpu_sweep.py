@@ -117,8 +117,9 @@ def test_rank_count_sweep(cuda, n, gd):
 def test_stage3_rank_count_sweep(cuda, n):
     """Stage 3 at several rank counts: random tensor lists in random layer
     groups, a per-group fused step in reverse order writing the owners' bf16
-    shards, then every group gathered (directly and by the two-stream pass)
-    and compared with the oracle's gather of the cast shards."""
+    shards, then every group gathered (directly, in the broadcast form and by
+    the two-stream pass) and compared with the oracle's gather and broadcast
+    of the cast shards."""
     import torch
     rng = np.random.default_rng(104729 * n)
     align = int(rng.choice([1, 2, 4, 8, 16]))
@@ -147,10 +148,15 @@ def test_stage3_rank_count_sweep(cuda, n):
         f0, S = g["flat_off"], g["shard"]
         own = [O.f32_to_bf16(c.h_master[f0 + k * S:f0 + (k + 1) * S]) for k in range(n)]
         want.append(O.gather_layer(own)[0])
+        want_b = O.broadcast_gather(own)[0]
         layer = torch.empty(max(1, g["psi_pad"]), dtype=torch.bfloat16, device=cuda)
         Z.zero_gather_layer(c.plan, gi, shards, Z.ZERO_BF16, layer)
         torch.cuda.synchronize()
         assert_bf16(bits_of(layer[:g["psi_pad"]]), want[gi], f"{what} layer {gi}")
+        layer.zero_()
+        Z.zero_broadcast_layer(c.plan, gi, shards, Z.ZERO_BF16, layer)
+        torch.cuda.synchronize()
+        assert_bf16(bits_of(layer[:g["psi_pad"]]), want_b, f"{what} broadcast layer {gi}")
     bufs = [torch.empty(max(1, gmax), dtype=torch.bfloat16, device=cuda) for _ in range(2)]
     order = list(range(G)) + list(reversed(range(G)))
     sums = torch.zeros(len(order), dtype=torch.int64, device=cuda)
