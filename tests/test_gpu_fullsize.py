@@ -105,8 +105,9 @@ def test_llama_1_4b_full_size_bucketed_clip(cuda):
 
 
 def test_llama_7b_stage3_full_size(cuda):
-    """Stage 3: per layer group (reverse order) a fused reduce-scatter + Adam
-    writing each owner's bf16 shard from a regenerated gradient slot; then
+    """Stage 3: two steps, each per layer group (reverse order) a fused
+    reduce-scatter + Adam writing each owner's bf16 shard from a regenerated
+    gradient slot; then
     forward and reverse per-layer gathers prefetched on a second stream while
     a consumer checksums the current layer.  Every gathered layer is compared
     element by element."""
@@ -122,19 +123,21 @@ def test_llama_7b_stage3_full_size(cuda):
     slot = [torch.empty(gmax, dtype=torch.bfloat16, device=cuda) for _ in range(N)]
     shards = [torch.zeros(c.info["shard_total"], dtype=torch.bfloat16, device=cuda)
               for _ in range(N)]
-    for gi in reversed(range(G)):
-        g = c.groups[gi]
-        views = [t[:g["psi_pad"]] for t in slot]
-        c.grads_dev(gi, 1, views)
-        Z.zero_step_group(c.plan, gi, views, Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(1), None,
-                          shards)
+    steps = (1, 2)                  # the second step starts from nonzero m and v
+    for s in steps:
+        for gi in reversed(range(G)):
+            g = c.groups[gi]
+            views = [t[:g["psi_pad"]] for t in slot]
+            c.grads_dev(gi, s, views)
+            Z.zero_step_group(c.plan, gi, views, Z.ZERO_BF16, c.master, c.m, c.v, c.hp_dev(s),
+                              None, shards)
     torch.cuda.synchronize()
     # sampled windows of every group: state and each owner's shard
     for gi, g in enumerate(c.groups):
         S, ro = g["shard"], g["rank_off"]
         wins = boundary_windows(g["psi_pad"], [k * S for k in range(1, N)], 256)
         for win in (wins if gi in (0, 1, G - 1) else wins[::5]):
-            r = c.oracle_window(gi, win, (1,))
+            r = c.oracle_window(gi, win, steps)
             c.check_window(gi, win, r, f"group {gi} {win}")
             full = O.f32_to_bf16(r["master"])
             for j in range(win[0], win[1], 64):
