@@ -216,6 +216,17 @@ int zero_rs_partials(const zero_plan_t* plan, zero_dtype_t gdtype, int64_t n_ele
 int zero_grad_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
                    float* d_coef, zero_stream_t stream);
 
+/* zero_adam_bias_corrections [KB, Algorithm 1: the bias corrections
+ * 1 - beta^t]: the two fp32 values the device calls use for hp->step, bc1 =
+ * 1 - beta1^t and bc2 = 1 - beta2^t, with beta^t the product of t fp64
+ * factors of the fp32 beta (each stopping once below 2^-60) rounded once to
+ * fp32.  Host only; touches no device.  Each host thread continues the
+ * product from its previous call when the step has not gone back (for
+ * growing step numbers the cost is one factor per step, not t), with results
+ * identical to the full product.  Errors: EINVAL (hp or an output NULL,
+ * invalid betas, step < 1). */
+int zero_adam_bias_corrections(const zero_adam_t* hp, float* bc1, float* bc2);
+
 /* zero_adam_state_init / zero_adam_state_advance: Adam's step-dependent
  * constants kept in device memory (no counterpart on the pages; it lets a
  * whole step be captured once in a CUDA graph and replayed).  d_state is a

@@ -425,3 +425,41 @@ def test_header_compiles_as_c99_and_library_links(tmp_path):
     assert lines[2] == "rank 1: (0 2512 2512 1584) (1 0 4096 928)"
     assert lines[5] == "stage2 17584 55264 volume 7536 7536"
     assert lines[6] == f"bad {Z.ZERO_EINVAL} invalid argument"
+
+
+def test_bias_corrections_match_the_oracle_for_any_step_order():
+    """The library's host bias corrections (which continue the beta^t product
+    from the thread's previous call) equal the oracle's full product for
+    growing steps, repeats, jumps back and forth, other betas in between, and
+    from several host threads at once."""
+    import threading
+    import numpy as np
+    from oracle import zero_oracle as O
+    rng = np.random.default_rng(5)
+    seq = list(range(1, 1501)) + [1500, 3, 3, 7000, 6999, 41_000, 42_500, 2, 1]
+    betas = [(0.9, 0.999)] * len(seq)
+    for i in rng.integers(0, len(seq), 40):                  # other betas in between
+        betas[i] = (0.8, 0.99)
+    for step, (b1, b2) in zip(seq, betas):
+        got = Z.zero_adam_bias_corrections(Z.adam_hp(step, 0.25, beta1=b1, beta2=b2))
+        want = O.bias_corrections(b1, b2, step)
+        assert np.float32(got[0]) == want[0] and np.float32(got[1]) == want[1], (step, b1, b2)
+    errors = []
+
+    def worker(b1, b2, steps):
+        for s in steps:
+            got = Z.zero_adam_bias_corrections(Z.adam_hp(s, 0.25, beta1=b1, beta2=b2))
+            want = O.bias_corrections(b1, b2, s)
+            if not (np.float32(got[0]) == want[0] and np.float32(got[1]) == want[1]):
+                errors.append((b1, b2, s))
+    ts = [threading.Thread(target=worker, args=(b1, b2, range(1, 400)))
+          for b1, b2 in [(0.9, 0.999), (0.95, 0.98), (0.5, 0.9)]]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors[:5]
+    for bad in (Z.adam_hp(0, 0.25), Z.adam_hp(1, 0.25, beta2=1.0)):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_adam_bias_corrections(bad)
+        assert e.value.status == Z.ZERO_EINVAL

@@ -139,6 +139,8 @@ _SIGS = {
     "zero_stage3_gather_pass_steps": (c_i32, [c_vp, P(c_i32), P(c_i32), c_i32, P(c_vp),
                                               P(c_vp), c_i64, c_vp, c_i32, c_vp, c_vp]),
     "zero_copy": (c_i32, [c_vp, c_vp, c_i64, c_vp]),
+    "zero_adam_bias_corrections": (c_i32, [P(zero_adam_t), P(ctypes.c_float),
+                                           P(ctypes.c_float)]),
     "zero_adam_state_init": (c_i32, [P(zero_adam_t), c_vp, c_vp]),
     "zero_adam_state_advance": (c_i32, [P(zero_adam_t), c_vp, c_vp]),
     "zero_set_occupancy": (c_i32, [c_i32, c_i32, P(c_i32)]),
@@ -638,6 +640,15 @@ def zero_layer_checksum(layer, n, rounds, d_out, stream=None) -> None:
     _need(d_out, 8, "d_out")
     _check(_lib().zero_layer_checksum(_ptr(layer), n, rounds, _ptr(d_out), _stream(stream)),
            "zero_layer_checksum")
+
+
+def zero_adam_bias_corrections(hp):
+    """(bc1, bc2): the fp32 bias corrections the device calls use for
+    hp.step (host only)."""
+    a, b = ctypes.c_float(), ctypes.c_float()
+    _check(_lib().zero_adam_bias_corrections(ctypes.byref(hp), ctypes.byref(a), ctypes.byref(b)),
+           "zero_adam_bias_corrections")
+    return a.value, b.value
 
 
 def zero_adam_state_init(hp, d_state, stream=None) -> None:

@@ -96,14 +96,39 @@ zk::RankPtrs rank_ptrs(const zero_plan_t* p, const void* const* ptrs) {
 // multiplications, each factor stopping once below 2^-60 (where 1 - beta^t
 // is exactly 1 in fp64).  The bias corrections are 1 - beta^t in fp64,
 // rounded once to fp32; (1 - beta) and lr*wd are fp32 operations.
+//
+// Training calls this with step numbers that grow by one, and the product
+// takes up to ~41 500 factors (0.999^t reaches 2^-60 only then), so each host
+// thread remembers where its last call ended for that pair of betas and
+// continues the same product from there when the step has not gone back: the
+// same multiplications in the same order, hence the same result.
+struct BetaPows {
+  float beta1 = -1.0f, beta2 = -1.0f;
+  int64_t step = 0;
+  double a = 1.0, b = 1.0;
+};
+thread_local BetaPows g_pows;
+
 void beta_pows(float beta1, float beta2, int64_t step, double* p1, double* p2) {
   double a = 1.0, b = 1.0;
+  int64_t t = 0;
+  BetaPows& c = g_pows;
+  if (c.beta1 == beta1 && c.beta2 == beta2 && c.step <= step) {
+    t = c.step;
+    a = c.a;
+    b = c.b;
+  }
   const double b1 = (double)beta1, b2 = (double)beta2;
   const double tiny = 8.673617379884035e-19;  // 2^-60
-  for (int64_t t = 0; t < step && (a >= tiny || b >= tiny); ++t) {
+  for (; t < step && (a >= tiny || b >= tiny); ++t) {
     if (a >= tiny) a *= b1;
     if (b >= tiny) b *= b2;
   }
+  c.beta1 = beta1;
+  c.beta2 = beta2;
+  c.step = step;
+  c.a = a;
+  c.b = b;
   *p1 = a;
   *p2 = b;
 }
@@ -491,6 +516,17 @@ extern "C" int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t m
   if (((uintptr_t)flag & 3u) != 0 || ((uintptr_t)d_status & 3u) != 0) return ZERO_EALIGN;
   return cuda_status(zk::launch_wait_flag(flag, expected, max_polls, d_status,
                                           (cudaStream_t)stream));
+}
+
+extern "C" int zero_adam_bias_corrections(const zero_adam_t* hp, float* bc1, float* bc2) {
+  if (!bc1 || !bc2) return ZERO_EINVAL;
+  ZERO_TRY(check_hp(hp));
+  if (hp->step < 1) return ZERO_EINVAL;
+  double p1 = 1.0, p2 = 1.0;
+  beta_pows(hp->beta1, hp->beta2, hp->step, &p1, &p2);
+  *bc1 = (float)(1.0 - p1);
+  *bc2 = (float)(1.0 - p2);
+  return ZERO_OK;
 }
 
 extern "C" int zero_adam_state_init(const zero_adam_t* hp, void* d_state, zero_stream_t stream) {
