@@ -321,6 +321,21 @@ int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* g
                     const zero_adam_t* hp, const float* d_coef, void* const* shards,
                     zero_stream_t stream);
 
+/* zero_step_group_acc (stage 3): the last micro-batch of gradient
+ * accumulation ["ZeRO Optimizer", "Hybrid Approaches": gradient accumulation
+ * with micro-batching] fused, as zero_step_acc is for stages 1 and 2: the
+ * reduced gradient is taken as accumulated[f] + (this micro-batch's ring
+ * sum), in that order, fp32, `accumulated` being the flat fp32 buffer that
+ * zero_reduce_scatter and zero_reduce_scatter_acc filled for the group's
+ * earlier micro-batches (read only); then scale, Adam and each owner's bf16
+ * parameters into its shard buffer, as zero_step_group.  hp->grad_scale is
+ * 1/(N * micro-batches).  `accumulated` must not overlap master, m or v; the
+ * same pointer in two of these roles returns ZERO_EINVAL. */
+int zero_step_group_acc(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                        zero_dtype_t gdtype, const float* accumulated, float* master, float* m,
+                        float* v, const zero_adam_t* hp, const float* d_coef,
+                        void* const* shards, zero_stream_t stream);
+
 /* zero_gather_layer (stage 3) [P4 "Implementation Strategy": gather a
  * layer's parameters just before use; P2: by all-gather]: layer_out[j] =
  * shards[j / S_g][rank_off(g) + j % S_g] for j in [0, psi_pad(g)): the N

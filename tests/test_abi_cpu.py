@@ -322,6 +322,12 @@ def test_device_call_argument_errors_return_before_any_launch():
                   A + 48) == Z.ZERO_EINVAL                  # accumulated is also the master
     assert status(Z.zero_step_acc, p, 0, good, Z.ZERO_BF16, A + 48, A, A + 16, A + 32, hp, None,
                   A + 48) == Z.ZERO_EINVAL                  # ... or the output
+    assert status(Z.zero_step_group_acc, p, 0, good, Z.ZERO_BF16, A + 32, A, A + 16, A + 32, hp,
+                  None, good) == Z.ZERO_EINVAL              # accumulated is also v
+    assert status(Z.zero_step_group_acc, p, 0, good, Z.ZERO_BF16, A + 8, A, A + 16, A + 32, hp,
+                  None, good) == Z.ZERO_EALIGN
+    assert status(Z.zero_step_group_acc, p, 1, good, Z.ZERO_BF16, A + 48, A, A + 16, A + 32, hp,
+                  None, good) == Z.ZERO_ERANGE
     assert status(Z.zero_gather_groups, p, [0], good, Z.ZERO_BF16, [A + 2]) == Z.ZERO_EALIGN
     assert status(Z.zero_gather_groups, p, [0, 1], good, Z.ZERO_BF16, [A, A]) == Z.ZERO_ERANGE
     assert status(Z.zero_gather_groups, p, [], good, Z.ZERO_BF16, []) == Z.ZERO_EINVAL

@@ -773,3 +773,54 @@ def test_gathers_queued_right_after_the_step_that_writes_their_shards(cuda):
         own = [O.f32_to_bf16(c.h_master[f0 + k * S:f0 + (k + 1) * S]) for k in range(N)]
         assert np.array_equal(bits_of(lay_a[gi]), O.gather_layer(own)[0]), ("graph", gi)
         assert np.array_equal(bits_of(lay_b[gi]), O.broadcast_gather(own)[0]), ("graph", gi)
+
+
+@pytest.mark.parametrize("gd", ["bf16", "f32"])
+def test_stage3_last_micro_batch_fused_into_the_group_step(cuda, gd):
+    """Stage 3 with gradient accumulation: per layer group the first micro-
+    batches go through zero_reduce_scatter / zero_reduce_scatter_acc into the
+    flat accumulation buffer, and the last one through zero_step_group_acc
+    (its ring sum added to the accumulated buffer inside the fused step,
+    owners' bf16 parameters into their shard buffers).  State and shards
+    equal the oracle's accumulation + Adam; the accumulated buffer is left as
+    it was."""
+    import torch
+    M = 3
+    d, ffn, vocab = 48, 130, 301
+    blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(2)]
+    numels = [vocab * d] + [n for b in blocks for n in b] + [d, vocab * d]
+    groups = [0] + [1 + i // 9 for i in range(18)] + [3, 3]
+    c = Case(numels, 8, 8, gd, grad_sigma=1e-2 if gd == "f32" else 1e-3, seed=41, groups=groups)
+    Z = c.Z
+    N, G = c.n, len(c.groups)
+    scale = 1.0 / (N * M)
+    acc = torch.full((c.info["psi_pad"],), 5.0, dtype=torch.float32, device=cuda)
+    shards = [torch.zeros(c.info["shard_total"], dtype=torch.bfloat16, device=cuda)
+              for _ in range(N)]
+    for gi in reversed(range(G)):
+        P = c.groups[gi]["psi_pad"]
+        Z.zero_reduce_scatter(c.plan, gi, c.grads_dev(gi, 50), c.zdtype, acc, 0, P, 1.0)
+        for k in range(1, M - 1):
+            Z.zero_reduce_scatter_acc(c.plan, gi, c.grads_dev(gi, 50 + k), c.zdtype, acc, 0, P,
+                                      1.0)
+    before = acc.clone()
+    hp = Z.adam_hp(step=1, grad_scale=scale)
+    for gi in reversed(range(G)):
+        Z.zero_step_group_acc(c.plan, gi, c.grads_dev(gi, 50 + M - 1), c.zdtype, acc, c.master,
+                              c.m, c.v, hp, None, shards)
+    torch.cuda.synchronize()
+    assert torch.equal(acc, before)
+    for gi, g in enumerate(c.groups):
+        f0, S, ro = g["flat_off"], g["shard"], g["rank_off"]
+        red = O.ring_reduce_scatter(c.grads_host(gi, 50), S)[0]
+        for k in range(1, M):
+            red = O.accumulate_reduced(red, O.ring_reduce_scatter(c.grads_host(gi, 50 + k), S)[0])
+        gs = O.scale(red, np.float32(scale))
+        sl = slice(f0, f0 + g["psi_pad"])
+        p, m, v = O.adam_update(c.h_master[sl], c.h_m[sl], c.h_v[sl], np.concatenate(gs), 1e-3,
+                                0.9, 0.999, 1e-8, 0.0, 1)
+        c.h_master[sl], c.h_m[sl], c.h_v[sl] = p, m, v
+        for k in range(N):
+            assert_bf16(bits_of(shards[k][ro:ro + S]), O.f32_to_bf16(p[k * S:(k + 1) * S]),
+                        f"group {gi} shard {k}")
+    c.check_state(f"stage 3 accumulation ({gd})")

@@ -130,6 +130,8 @@ _SIGS = {
                               P(zero_adam_t), c_vp, c_vp, c_i32, c_vp]),
     "zero_step_group": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp,
                                 P(zero_adam_t), c_vp, P(c_vp), c_vp]),
+    "zero_step_group_acc": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp, c_vp, c_vp,
+                                    P(zero_adam_t), c_vp, P(c_vp), c_vp]),
     "zero_gather_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
     "zero_broadcast_layer": (c_i32, [c_vp, c_i32, P(c_vp), c_i32, c_vp, c_vp]),
     "zero_gather_groups": (c_i32, [c_vp, P(c_i32), c_i32, P(c_vp), c_i32, P(c_vp), c_vp]),
@@ -562,6 +564,21 @@ def zero_step_group(plan, group, grads, gdtype, master, m, v, hp, d_coef, shards
     _check(_lib().zero_step_group(plan, group, grad_ptrs, gdtype, _ptr(master), _ptr(m),
                                   _ptr(v), ctypes.byref(hp), _ptr(d_coef), shard_ptrs,
                                   _stream(stream)), "zero_step_group")
+
+
+def zero_step_group_acc(plan, group, grads, gdtype, accumulated, master, m, v, hp, d_coef,
+                        shards, stream=None) -> None:
+    g, es = _group(plan, group), _ESIZE.get(gdtype, 0)
+    if g is not None:
+        for x, what in ((accumulated, "accumulated"), (master, "master"), (m, "m"), (v, "v")):
+            _need(x, (g[0] + g[1]) * 4, what)
+    _need(d_coef, 4, "d_coef")
+    grad_ptrs = _ranks(plan, grads, "grads", g[1] * es if g else 0)
+    shard_ptrs = _ranks(plan, shards, "shards", plan.geometry()["shard_total"] * 2)
+    _check(_lib().zero_step_group_acc(plan, group, grad_ptrs, gdtype, _ptr(accumulated),
+                                      _ptr(master), _ptr(m), _ptr(v), ctypes.byref(hp),
+                                      _ptr(d_coef), shard_ptrs, _stream(stream)),
+           "zero_step_group_acc")
 
 
 def zero_gather_layer(plan, group, shards, dtype, layer_out, stream=None) -> None:

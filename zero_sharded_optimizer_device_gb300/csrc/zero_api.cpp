@@ -413,11 +413,13 @@ extern "C" int zero_step_acc(const zero_plan_t* plan, int32_t group, const void*
                     out_dtype, stream);
 }
 
-extern "C" int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* grads,
-                               zero_dtype_t gdtype, float* master, float* m, float* v,
-                               const zero_adam_t* hp, const float* d_coef, void* const* shards,
-                               zero_stream_t stream) {
-  NvtxRange nvtx("zero_step_group");
+// The stage-3 fused step: owner k writes its updated bf16 parameters into its
+// own shard buffer; prev (may be NULL) is the accumulated reduced gradient of
+// earlier micro-batches.
+static int group_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                      zero_dtype_t gdtype, const float* prev, float* master, float* m, float* v,
+                      const zero_adam_t* hp, const float* d_coef, void* const* shards,
+                      zero_stream_t stream) {
   ZERO_TRY(check_group(plan, group));
   if (!dtype_ok(gdtype)) return ZERO_EDTYPE;
   ZERO_TRY(check_rank_ptrs(plan, grads));
@@ -430,9 +432,34 @@ extern "C" int zero_step_group(const zero_plan_t* plan, int32_t group, const voi
   ZERO_TRY(adam_k(hp, &k));
   zk::OutPtrs out{};
   for (int r = 0; r < plan->n_ranks; ++r) out.p[r] = shards[r];
-  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), fused_gdtype(plan, gdtype, grads), group_k(plan, group), 0,
-                                      plan->groups[group].psi_pad, master, m, v, k, d_coef, nullptr,
-                                      zk::OUT_SHARDS_BF16, nullptr, out, (cudaStream_t)stream));
+  return cuda_status(zk::launch_fused(rank_ptrs(plan, grads), fused_gdtype(plan, gdtype, grads),
+                                      group_k(plan, group), 0, plan->groups[group].psi_pad,
+                                      master, m, v, k, d_coef, prev, zk::OUT_SHARDS_BF16,
+                                      nullptr, out, (cudaStream_t)stream));
+}
+
+extern "C" int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* grads,
+                               zero_dtype_t gdtype, float* master, float* m, float* v,
+                               const zero_adam_t* hp, const float* d_coef, void* const* shards,
+                               zero_stream_t stream) {
+  NvtxRange nvtx("zero_step_group");
+  return group_step(plan, group, grads, gdtype, nullptr, master, m, v, hp, d_coef, shards,
+                    stream);
+}
+
+extern "C" int zero_step_group_acc(const zero_plan_t* plan, int32_t group,
+                                   const void* const* grads, zero_dtype_t gdtype,
+                                   const float* accumulated, float* master, float* m, float* v,
+                                   const zero_adam_t* hp, const float* d_coef,
+                                   void* const* shards, zero_stream_t stream) {
+  NvtxRange nvtx("zero_step_group_acc");
+  ZERO_TRY(check_buf(accumulated));
+  // read through a restrict pointer while the state is written: one buffer in
+  // two roles is refused
+  const void* acc = accumulated;
+  if (acc == master || acc == m || acc == v) return ZERO_EINVAL;
+  return group_step(plan, group, grads, gdtype, accumulated, master, m, v, hp, d_coef, shards,
+                    stream);
 }
 
 extern "C" int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
