@@ -469,3 +469,23 @@ def test_bias_corrections_match_the_oracle_for_any_step_order():
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_adam_bias_corrections(bad)
         assert e.value.status == Z.ZERO_EINVAL
+
+
+def test_binding_refuses_tensors_of_another_device(monkeypatch):
+    """The library launches on the current device, so a tensor that lives on
+    another GPU is refused before any call (it would be an illegal address
+    there).  Host-only: the current device and the tensor are stand-ins."""
+    import torch
+
+    class OtherGpuTensor:
+        is_cuda = True
+        device = torch.device("cuda", 1)
+
+        def data_ptr(self):
+            return 1 << 40
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    with pytest.raises(ValueError, match="cuda:1 passed while cuda:0"):
+        Z.binding._ptr(OtherGpuTensor())
+    OtherGpuTensor.device = torch.device("cuda", 0)
+    assert Z.binding._ptr(OtherGpuTensor()) == 1 << 40

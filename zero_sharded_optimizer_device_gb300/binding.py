@@ -229,15 +229,22 @@ def _host_memory_reachable(addr: int) -> bool:
 
 
 def _ptr(x) -> int | None:
-    """Address of a tensor the GPU can reach (a CUDA tensor, or a CPU tensor
-    in host memory the device can dereference); raw integer addresses pass as
-    they are."""
+    """Address of a tensor the GPU can reach (a CUDA tensor on the current
+    device, or a CPU tensor in host memory the device can dereference); raw
+    integer addresses pass as they are."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
     addr = x.data_ptr()
-    if not x.is_cuda and not (x.is_pinned() or _host_memory_reachable(addr)):
+    if x.is_cuda:
+        # the library launches on the current device: another device's memory
+        # would be an illegal address there
+        import torch
+        if x.device.index != torch.cuda.current_device():
+            raise ValueError(f"a tensor on {x.device} passed while cuda:"
+                             f"{torch.cuda.current_device()} is the current device")
+    elif not (x.is_pinned() or _host_memory_reachable(addr)):
         raise ValueError("a CPU tensor in pageable host memory is not device-accessible here: "
                          "use a CUDA tensor or page-locked (pinned) host memory")
     return addr
