@@ -33,7 +33,8 @@
  *     passed as zero_stream_t; NULL = the legacy default stream).  They
  *     report argument errors and launch errors only; a later
  *     cudaStreamSynchronize reports execution errors.
- *   - "Device pointer" means any address the GPU can access: device memory,
+ *   - Calls launch on the calling thread's current CUDA device.
+ *   - "Device pointer" means any address that device can access: its memory,
  *     pinned host memory mapped into the device address space (cudaHostAlloc
  *     on a unified-addressing system), or -- where the device reports
  *     cudaDevAttrPageableMemoryAccess, as a GB300 behind NVLink-C2C does --
