@@ -154,24 +154,28 @@ int zero_plan_destroy(zero_plan_t* plan);
 int zero_plan_info(const zero_plan_t* plan, zero_plan_info_t* out);
 int zero_plan_group(const zero_plan_t* plan, int32_t group, zero_group_info_t* out);
 /* Flat offset of tensor t and the ranks owning its first and last element
- * (-1 for an empty tensor). */
+ * (-1 for an empty tensor).  Errors: EINVAL (plan NULL), ERANGE (t outside
+ * the plan). */
 int zero_plan_tensor(const zero_plan_t* plan, int64_t t, int64_t* flat_off,
                      int32_t* first_owner, int32_t* last_owner);
 /* Rank r's shard of group g: flat begin, length S_g, real (non-padding)
- * elements. */
+ * elements.  Errors: EINVAL (plan NULL), ERANGE (group or rank outside the
+ * plan). */
 int zero_plan_shard(const zero_plan_t* plan, int32_t group, int32_t rank, int64_t* begin,
                     int64_t* len, int64_t* valid_len);
 /* Pieces of tensors rank r owns, in flat order.  Writes min(cap, count)
- * entries to out (out may be NULL when cap == 0); *n = count. */
+ * entries to out (out may be NULL when cap == 0); *n = count.  Errors:
+ * EINVAL (plan or n NULL, cap < 0, out NULL with cap > 0), ERANGE (rank). */
 int zero_plan_segments(const zero_plan_t* plan, int32_t rank, zero_seg_t* out, int64_t cap,
                        int64_t* n);
 /* Per-device memory of stage 0 (plain data parallelism: 4P values [P4
  * "Memory Components"]), 1 (2P + 2P/N), 2 (P + 3P/N) or 3 (4P/N) [P4
  * "Theoretical Reductions"], with P = psi_pad and P/N = shard_total; bytes
- * count bf16 params and grads and 12 bytes of fp32 master + m + v. */
+ * count bf16 params and grads and 12 bytes of fp32 master + m + v.
+ * Errors: EINVAL (plan or out NULL), ERANGE (stage not 0..3). */
 int zero_plan_memory(const zero_plan_t* plan, int32_t stage, zero_mem_t* out);
 /* Elements each rank sends and receives in one ring reduce-scatter (and in
- * one all-gather): (N-1) * shard_total [P3]. */
+ * one all-gather): (N-1) * shard_total [P3].  Errors: EINVAL (plan NULL). */
 int zero_plan_volume(const zero_plan_t* plan, int64_t* send_per_rank, int64_t* recv_per_rank);
 
 /* ------------------------------------------------------- device calls -- */
@@ -198,14 +202,17 @@ int zero_reduce_scatter(const zero_plan_t* plan, int32_t group, const void* cons
  * in that order, fp32, for i in [begin, end).  The first micro-batch uses
  * zero_reduce_scatter; Adam then takes grad_scale = 1/(N * micro_batches).
  * sumsq_partials (may be NULL) sum (accumulated * grad_scale)^2, so the last
- * micro-batch's call yields the norm of the accumulated gradient. */
+ * micro-batch's call yields the norm of the accumulated gradient.
+ * Errors: EINVAL, EALIGN, ERANGE, EDTYPE, ECUDA (as zero_reduce_scatter;
+ * reduced is required). */
 int zero_reduce_scatter_acc(const zero_plan_t* plan, int32_t group, const void* const* grads,
                             zero_dtype_t gdtype, float* reduced, int64_t begin, int64_t end,
                             float grad_scale, double* sumsq_partials, zero_stream_t stream);
 
 /* Number of fp64 partials zero_reduce_scatter writes for a window of
  * n_elements with this plan's N and gdtype on the current device (one per
- * block of its launch; blocks without work write 0). */
+ * block of its launch; blocks without work write 0).  Errors: EINVAL (plan
+ * or n_partials NULL, n_elements < 0), EDTYPE. */
 int zero_rs_partials(const zero_plan_t* plan, zero_dtype_t gdtype, int64_t n_elements,
                      int64_t* n_partials);
 
@@ -213,7 +220,9 @@ int zero_rs_partials(const zero_plan_t* plan, zero_dtype_t gdtype, int64_t n_ele
  * order; coef = min(1, max_norm / (norm + 1e-6)) rounded to fp32.  Writes
  * *d_norm (fp32) and *d_coef (fp32) on the device; either may be NULL.
  * The clip is not on the pages; it is the coefficient torch's
- * clip_grad_norm_ applies. */
+ * clip_grad_norm_ applies.  Errors: EINVAL (n < 0, partials NULL with n > 0,
+ * max_norm not finite and positive), EALIGN (partials not 8-byte, outputs
+ * not 4-byte aligned), ECUDA. */
 int zero_grad_norm(const double* partials, int64_t n, float max_norm, float* d_norm,
                    float* d_coef, zero_stream_t stream);
 
@@ -283,7 +292,8 @@ int zero_step_clipped(const zero_plan_t* plan, int32_t group, const void* const*
 /* zero_all_gather [P1 "Problem"; P3 all-gather]: full_out[f] = cast(
  * master[f]) for every element of group g (g = -1: all groups), i.e. every
  * owner's updated shard lands in the one full flat parameter buffer all
- * ranks share.  out_dtype: ZERO_BF16 (round to nearest even) or ZERO_F32. */
+ * ranks share.  out_dtype: ZERO_BF16 (round to nearest even) or ZERO_F32.
+ * Errors: EINVAL, EALIGN, ERANGE (group), EDTYPE, ECUDA. */
 int zero_all_gather(const zero_plan_t* plan, int32_t group, const float* master,
                     void* full_out, zero_dtype_t out_dtype, zero_stream_t stream);
 
@@ -291,7 +301,8 @@ int zero_all_gather(const zero_plan_t* plan, int32_t group, const float* master,
  * all-gather of group g in one pass; the reduced gradient never reaches
  * memory.  Same arithmetic, per element, as zero_reduce_scatter followed by
  * zero_adam_shard with out = full_out (bit-identical results).  full_out
- * may be NULL (no gather). */
+ * may be NULL (no gather).  Errors: EINVAL (NULL or invalid arguments, Adam
+ * hyperparameters), EALIGN, ERANGE (group), EDTYPE, ECUDA. */
 int zero_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
               zero_dtype_t gdtype, float* master, float* m, float* v, const zero_adam_t* hp,
               const float* d_coef, void* full_out, zero_dtype_t out_dtype,
@@ -308,7 +319,7 @@ int zero_step(const zero_plan_t* plan, int32_t group, const void* const* grads,
  * gradient (8 bytes per parameter less).  hp->grad_scale is 1/(N * micro-batches).
  * `accumulated` must not overlap master, m, v or full_out (the kernel reads it
  * while writing those); the same pointer in two of these roles returns
- * ZERO_EINVAL. */
+ * ZERO_EINVAL.  Errors: as zero_step. */
 int zero_step_acc(const zero_plan_t* plan, int32_t group, const void* const* grads,
                   zero_dtype_t gdtype, const float* accumulated, float* master, float* m,
                   float* v, const zero_adam_t* hp, const float* d_coef, void* full_out,
@@ -316,7 +327,9 @@ int zero_step_acc(const zero_plan_t* plan, int32_t group, const void* const* gra
 
 /* zero_step_group (stage 3) [P4 "ZeRO Stages", stage 3]: as zero_step, but
  * each owner writes its updated bf16 parameters only into its own shard
- * buffer: shards[k][rank_off(g) + (i - k*S_g)] for owner k of element i. */
+ * buffer: shards[k][rank_off(g) + (i - k*S_g)] for owner k of element i.
+ * Errors: EINVAL (NULL or invalid arguments, Adam hyperparameters), EALIGN,
+ * ERANGE (group), EDTYPE, ECUDA. */
 int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* grads,
                     zero_dtype_t gdtype, float* master, float* m, float* v,
                     const zero_adam_t* hp, const float* d_coef, void* const* shards,
@@ -331,7 +344,8 @@ int zero_step_group(const zero_plan_t* plan, int32_t group, const void* const* g
  * earlier micro-batches (read only); then scale, Adam and each owner's bf16
  * parameters into its shard buffer, as zero_step_group.  hp->grad_scale is
  * 1/(N * micro-batches).  `accumulated` must not overlap master, m or v; the
- * same pointer in two of these roles returns ZERO_EINVAL. */
+ * same pointer in two of these roles returns ZERO_EINVAL.  Errors: as
+ * zero_step_group. */
 int zero_step_group_acc(const zero_plan_t* plan, int32_t group, const void* const* grads,
                         zero_dtype_t gdtype, const float* accumulated, float* master, float* m,
                         float* v, const zero_adam_t* hp, const float* d_coef,
@@ -349,7 +363,8 @@ int zero_step_group_acc(const zero_plan_t* plan, int32_t group, const void* cons
  * launch: its CTAs may become resident while the kernel before it on the
  * stream is still running, but they copy only after that kernel has finished
  * and its writes are visible, so stream order holds as for any launch (also
- * inside a captured CUDA graph). */
+ * inside a captured CUDA graph).  Errors: EINVAL, EALIGN, ERANGE (group),
+ * EDTYPE, ECUDA. */
 int zero_gather_layer(const zero_plan_t* plan, int32_t group, const void* const* shards,
                       zero_dtype_t dtype, void* layer_out, zero_stream_t stream);
 
@@ -425,7 +440,8 @@ int zero_stage3_gather_pass(const zero_plan_t* plan, const int32_t* order, int32
  * separate groups fetched together.  In a step of more than one group every
  * group's psi_pad * 2 bytes must be a multiple of 16 (ZERO_EALIGN otherwise),
  * and each step's elements must fit buf_elems (ZERO_ERANGE).  Otherwise as
- * zero_stage3_gather_pass. */
+ * zero_stage3_gather_pass, errors included (EINVAL also for a step of 0 or
+ * more than ZERO_MAX_COALESCE groups, or step_first[0] != 0). */
 int zero_stage3_gather_pass_steps(const zero_plan_t* plan, const int32_t* step_first,
                                   const int32_t* step_groups, int32_t n_steps,
                                   const void* const* shards, void* const* layer_bufs,
@@ -440,7 +456,10 @@ int zero_stage3_gather_pass_steps(const zero_plan_t* plan, const int32_t* step_f
  * rounds - 1 dependent multiply-adds t = t*K + c_v with K =
  * 6364136223846793005; *d_out = sum of the terms mod 2^64.  rounds = 1 is
  * the plain checksum, bound by the one read of the layer; larger rounds add
- * on-chip work only.  1 <= rounds <= ZERO_MAX_CONSUMER_ROUNDS. */
+ * on-chip work only.  1 <= rounds <= ZERO_MAX_CONSUMER_ROUNDS.  Errors:
+ * EINVAL (n < 0, d_out NULL, layer NULL with n > 0, rounds outside
+ * [1, ZERO_MAX_CONSUMER_ROUNDS]), EALIGN (layer not 16-byte, d_out not
+ * 8-byte aligned), ECUDA. */
 #define ZERO_MAX_CONSUMER_ROUNDS 4096
 int zero_layer_checksum(const void* layer, int64_t n, int32_t rounds, uint64_t* d_out,
                         zero_stream_t stream);
@@ -486,7 +505,9 @@ int zero_reduce_scatter_norm_static(const zero_plan_t* plan, int32_t group,
  * peer that never signals turns into a status the host reads after the
  * stream synchronizes, and the context stays usable.  0 <= max_polls <=
  * ZERO_MAX_POLLS (about 10 s).  Never use it to wait for another kernel of
- * this process: launches are not guaranteed to run concurrently. */
+ * this process: launches are not guaranteed to run concurrently.  Errors:
+ * EINVAL (NULL pointer, max_polls outside [0, ZERO_MAX_POLLS]), EALIGN (flag
+ * or d_status not 4-byte aligned), ECUDA (launch). */
 #define ZERO_MAX_POLLS 10000000
 int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
                    int32_t* d_status, zero_stream_t stream);
@@ -499,7 +520,8 @@ int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
  * and the best value depends on the kernel and the GPU.  *previous (may be
  * NULL) receives the value in effect before the call.  Process-wide; set it
  * between steps, not while a reduce-scatter's partials are still to be
- * read: zero_rs_partials() follows the setting in effect. */
+ * read: zero_rs_partials() follows the setting in effect.  Errors: EINVAL
+ * (kind or blocks_per_sm out of range). */
 #define ZERO_OCC_FUSED 0  /* zero_step, zero_step_group */
 #define ZERO_OCC_RS 1     /* zero_reduce_scatter, zero_reduce_scatter_acc */
 #define ZERO_OCC_ADAM 2   /* zero_adam_shard */
@@ -511,7 +533,9 @@ int zero_wait_flag(const uint32_t* flag, uint32_t expected, int64_t max_polls,
 int zero_set_occupancy(int32_t kind, int32_t blocks_per_sm, int32_t* previous);
 
 /* zero_copy: device-to-device copy of `bytes` (a multiple of 16) with
- * 16-byte loads and stores; measures the achievable HBM copy bandwidth. */
+ * 16-byte loads and stores; measures the achievable HBM copy bandwidth.
+ * bytes == 0 is a no-op.  Errors: EINVAL (bytes < 0 or not a multiple of 16,
+ * NULL pointer), EALIGN, ECUDA. */
 int zero_copy(void* dst, const void* src, int64_t bytes, zero_stream_t stream);
 
 /* zero_async_status: number of bounded waits inside the library's kernels
@@ -565,7 +589,8 @@ int zero_bounds_report(zero_bounds_t* out, int32_t reset);
 /* zero_bounds_probe: checked build only (a no-op returning ZERO_OK in the
  * release build): a one-thread kernel that makes no memory access and
  * records one out-of-extent access at ZERO_SITE_PROBE (index 1, extent
- * [0, 1)), so a caller can confirm the record reaches the host. */
+ * [0, 1)), so a caller can confirm the record reaches the host.  Errors:
+ * ECUDA (launch, checked build only). */
 int zero_bounds_probe(zero_stream_t stream);
 
 #ifdef __cplusplus
