@@ -511,6 +511,25 @@ def test_planted_mistakes_fail_a_pin(monkeypatch):
     assert np.array_equal(layer, np.concatenate(shards))
     assert not np.array_equal(layer, np.concatenate(shards[::-1]))
 
+    # a broadcast whose root also sends to itself: the per-broadcast counter
+    # pin ((N - 1) * S from the root) and the all-gather total pin both fail
+    _, _, sent, recv = O.broadcast_gather(shards)
+    n_, S_ = len(shards), len(shards[0])
+    self_send = [[n_ * S_ if r == k else 0 for r in range(n_)] for k in range(n_)]
+    assert sent != self_send
+    assert [sum(x[r] for x in self_send) for r in range(n_)] != O.gather_layer(shards)[1]
+    assert [sum(x[r] for x in sent) for r in range(n_)] == O.gather_layer(shards)[1]
+
+    # a norm that sums |g| instead of g*g, or squares in fp32 before the fp64
+    # sum: the exact integer pin of sum_squares
+    ints = [np.array([3, -4, 12], np.float32), np.array([4097], np.float32)]
+    exact = 9.0 + 16.0 + 144.0 + 4097.0 ** 2
+    assert O.sum_squares(ints) == exact
+    assert sum(float(np.abs(x).sum()) for x in ints) != exact
+    g1 = np.float32(1.0 + 2.0 ** -23)                           # (1 + 2^-23)^2 needs 47 bits
+    assert float(np.float32(g1 * g1)) != (1.0 + 2.0 ** -23) ** 2
+    assert O.sum_squares([np.array([g1], np.float32)]) == (1.0 + 2.0 ** -23) ** 2
+
 
 def test_accumulation_over_micro_batches():
     # exact arithmetic: accumulating M micro-batches' reduce-scatters equals
