@@ -555,3 +555,36 @@ def test_accumulation_over_micro_batches():
     k = n * M - 1
     gamma = k * 2.0 ** -24 / (1 - k * 2.0 ** -24)
     assert np.all(np.abs(np.concatenate(acc).astype(np.float64) - exact) <= gamma * absum)
+
+
+def test_golden_norm_script_window_and_file():
+    """The script that wrote tests/golden/llama_1_4b_norm.txt: its per-window
+    sum of squares is the oracle's ring reduce-scatter, 1/N scale and fp64
+    sum of squares over that window (a window across the owner 0/1 boundary),
+    and the stored norms and coefficients agree with each other."""
+    import importlib.util
+    import math
+    import os
+    import synth
+    from synth import workloads as W
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    spec = importlib.util.spec_from_file_location("make_norm",
+                                                  os.path.join(here, "make_llama_1_4b_norm.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    w = W.LLAMA_1_4B
+    p = O.plan(w.numels, w.n_ranks, w.align)
+    S = p.groups[0].shard
+    a, b = S - 700, S + 900
+    local = [O.bf16_to_f32(synth.values(w.seed, synth.GRAD, 2, r, a, b, w.grad_sigma, w.psi,
+                                        True, synth.DTYPE_BF16)) for r in range(w.n_ranks)]
+    red, _, _ = O.ring_reduce_scatter(local, S, (a, b))
+    want = O.sum_squares(O.scale(red, F32(1.0) / F32(w.n_ranks)))
+    assert mod.window_sum_squares((2, a, b)) == want
+    gold = read_golden("llama_1_4b_norm.txt")
+    assert int(gold["psi_pad"]) == p.psi_pad
+    for s in (1, 2):
+        norm = float(gold[f"norm_step{s}"])
+        assert norm == math.sqrt(float(gold[f"sumsq_step{s}"]))
+        assert float(gold[f"coef_step{s}"]) == float(O.clip_coef(norm, w.extra["max_norm"]))
+        assert 100.0 < norm < 200.0          # heavy tails: the clip at 1.0 is active
