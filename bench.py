@@ -209,8 +209,8 @@ def gpu_numa_node(dev_index: int):
         path = (f"/sys/bus/pci/devices/{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:"
                 f"{pr.pci_device_id:02x}.0/numa_node")
         node = int(open(path).read().strip())
-    except (OSError, ValueError, AttributeError):
-        return None
+    except (OSError, ValueError, AttributeError, RuntimeError, AssertionError):
+        return None                 # no device, or the kernel reports no node
     return node if node >= 0 else None
 
 

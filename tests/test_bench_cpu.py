@@ -94,3 +94,43 @@ def test_overlap_fraction():
     assert bench._hidden(10.0, 30.0, 30.0) == 1.0     # gathers entirely behind the consumer
     assert bench._hidden(10.0, 30.0, 40.0) == 0.0     # one after the other
     assert bench._hidden(8.0, 4.0, 10.0) == 0.5
+
+
+def test_host_placement_helpers_fail_soft_without_a_gpu():
+    """The end-to-end leg's placement helpers: the GPU's NUMA node is None
+    when there is no device to ask, the default memory policy can always be
+    restored, and the local rank count follows LOCAL_WORLD_SIZE."""
+    import os
+    assert bench.gpu_numa_node(0) is None or isinstance(bench.gpu_numa_node(0), int)
+    assert bench._set_mempolicy(None) in (True, False)
+    old = os.environ.get("LOCAL_WORLD_SIZE")
+    try:
+        os.environ["LOCAL_WORLD_SIZE"] = "4"
+        assert bench.local_ranks() == 4
+        os.environ["LOCAL_WORLD_SIZE"] = "0"
+        assert bench.local_ranks() == 1
+    finally:
+        if old is None:
+            os.environ.pop("LOCAL_WORLD_SIZE", None)
+        else:
+            os.environ["LOCAL_WORLD_SIZE"] = old
+
+
+def test_traffic_records_match_the_current_kernel_sources():
+    """Every DRAM traffic record in profiles/traffic.json was taken on the
+    kernel sources the repository holds now (the bench reports a record only
+    while the source hash matches), and carries the command that made it."""
+    import json
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    seen = 0
+    for workload, kernels in rec.items():
+        for key, entry in kernels.items():
+            kernel = key.replace("_block", "").replace("_step", "")
+            assert entry["source_hash"] == bench.kernel_source_hash(kernel), (workload, key)
+            assert entry["bytes_per_launch"] > 0
+            if not key.endswith("_step"):
+                assert entry["command"].startswith("ncu ") and "--clock-control none" in \
+                    entry["command"], (workload, key)
+            seen += 1
+    assert seen >= 8
