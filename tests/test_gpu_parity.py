@@ -91,6 +91,61 @@ def test_plain_c_program_drives_the_step(cuda, tmp_path):
     assert_bf16(got_out, r["full"], "C program gathered")
 
 
+def test_plain_c_program_drives_a_stage3_step(cuda, tmp_path):
+    """A C11 program with its own cudaMalloc'd buffers and streams runs one
+    stage-3 step (per-group fused steps writing owner shards), gathers every
+    layer directly and by the two-stream prefetch pass; its master weights,
+    layers and the pass's checksums equal the oracle's, bit for bit."""
+    import os
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    lib_dir = os.path.join(root, "zero_sharded_optimizer_device_gb300")
+    cuda_home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    exe = str(tmp_path / "c_abi_stage3")
+    cc = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror",
+                         "-I", os.path.join(root, "include"), "-I", f"{cuda_home}/include",
+                         os.path.join(root, "tests", "c_abi_stage3.c"), "-L", lib_dir, "-lzero",
+                         "-L", f"{cuda_home}/lib64", "-lcudart", f"-Wl,-rpath,{lib_dir}",
+                         f"-Wl,-rpath,{cuda_home}/lib64", "-o", exe],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    d, ffn, vocab = 48, 130, 301
+    blocks = [[d * d] * 4 + [d * ffn] * 2 + [ffn * d, d, d] for _ in range(2)]
+    numels = [vocab * d] + [x for b in blocks for x in b] + [d, vocab * d]
+    groups = [0] + [1 + i // 9 for i in range(18)] + [3, 3]
+    N = 8
+    c = Case(numels, N, 16, "f32", grad_sigma=1e-2, seed=97, groups=groups)
+    G, P = len(c.groups), c.info["psi_pad"]
+    parts = [np.array([N, len(numels)], np.int32).tobytes(), np.array(numels, np.int64).tobytes(),
+             np.array(groups, np.int32).tobytes()]
+    for gi in range(G):
+        parts += [x.astype(np.float32).tobytes() for x in c.grads_host(gi, 1)]
+    parts.append(c.h_master.astype(np.float32).tobytes())
+    inp = tmp_path / "in.bin"
+    inp.write_bytes(b"".join(parts))
+    outp = tmp_path / "out.bin"
+    run = subprocess.run([exe, str(inp), str(outp)], capture_output=True, text=True)
+    assert run.returncode == 0, (run.returncode, run.stderr)
+    raw = outp.read_bytes()
+    for gi in reversed(range(G)):
+        c.oracle_step(gi, 1)
+    assert_close_f32(np.frombuffer(raw[:4 * P], np.float32), c.h_master, "C program master")
+    off = 4 * P
+    layers = []
+    for gi, g in enumerate(c.groups):
+        f0, S = g["flat_off"], g["shard"]
+        own = [O.f32_to_bf16(c.h_master[f0 + k * S:f0 + (k + 1) * S]) for k in range(N)]
+        layers.append(O.gather_layer(own)[0])
+        got = np.frombuffer(raw[off:off + 2 * g["psi_pad"]], np.uint16)
+        off += 2 * g["psi_pad"]
+        assert np.array_equal(got, layers[gi]), gi
+    sums = np.frombuffer(raw[off:], np.uint64)
+    order = list(range(G)) + list(reversed(range(G)))
+    assert len(sums) == len(order)
+    for j, gi in enumerate(order):
+        assert int(sums[j]) == O.layer_checksum(layers[gi], 1), (j, gi)
+
+
 def test_tiny_unfused_chain(cuda):
     import torch
     w = W.TINY
