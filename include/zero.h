@@ -280,6 +280,9 @@ int zero_adam_shard(const zero_plan_t* plan, int32_t group, float* master, float
  *     (may be NULL) in out_dtype.
  * partials: caller-owned fp64 scratch of n_partials >= the count
  * zero_step_clipped_partials reports (ERANGE otherwise).  bucket, chunk >= 1.
+ * The call fixes its reduce-scatter grids before the first launch, so it
+ * writes exactly the partials it checked, even if zero_set_occupancy runs
+ * on another host thread meanwhile.
  * Errors: EINVAL, EALIGN, ERANGE, EDTYPE, ECUDA. */
 int zero_step_clipped_partials(const zero_plan_t* plan, int32_t group, zero_dtype_t gdtype,
                                int64_t bucket, int64_t* n_partials);

@@ -280,15 +280,28 @@ extern "C" int zero_adam_shard(const zero_plan_t* plan, int32_t group, float* ma
                                      d_coef, mode, out, (cudaStream_t)stream));
 }
 
-// Norm partials the clipped step writes: one zero_rs_partials() count per
-// reduce-scatter window of `bucket` elements.
+// The clipped step's reduce-scatter windows: every window but the last has
+// `bucket` elements, so two grids describe them all.  The grids are fixed
+// once per call and each window is launched with its stored grid, so the
+// partial count written equals the count checked even if another host thread
+// changes the occupancy setting meanwhile.
+struct ClippedGrids {
+  int64_t windows = 0, full = 0, last = 0;
+  int64_t total() const { return windows > 0 ? (windows - 1) * full + last : 0; }
+};
+static ClippedGrids clipped_grids(const zero_plan_t* plan, int32_t group, int gdtype,
+                                  int64_t bucket) {
+  const int64_t P = plan->groups[group].psi_pad;
+  ClippedGrids c;
+  if (P <= 0) return c;
+  c.windows = (P + bucket - 1) / bucket;
+  c.full = zk::rs_partials_for(plan->n_ranks, gdtype, bucket < P ? bucket : P);
+  c.last = zk::rs_partials_for(plan->n_ranks, gdtype, P - (c.windows - 1) * bucket);
+  return c;
+}
 static int64_t clipped_partials(const zero_plan_t* plan, int32_t group, int gdtype,
                                 int64_t bucket) {
-  const int64_t P = plan->groups[group].psi_pad;
-  int64_t n = 0;
-  for (int64_t a = 0; a < P; a += bucket)
-    n += zk::rs_partials_for(plan->n_ranks, gdtype, (P - a < bucket ? P - a : bucket));
-  return n;
+  return clipped_grids(plan, group, gdtype, bucket).total();
 }
 
 extern "C" int zero_step_clipped_partials(const zero_plan_t* plan, int32_t group,
@@ -324,19 +337,22 @@ extern "C" int zero_step_clipped(const zero_plan_t* plan, int32_t group, const v
   ZERO_TRY(check_opt_f32(d_coef));
   zk::AdamK k;
   ZERO_TRY(adam_k(hp, &k));
-  if (n_partials < clipped_partials(plan, group, gdtype, bucket)) return ZERO_ERANGE;
+  const ClippedGrids grids = clipped_grids(plan, group, gdtype, bucket);
+  if (n_partials < grids.total()) return ZERO_ERANGE;
   const cudaStream_t st = (cudaStream_t)stream;
   const zk::RankPtrs src = rank_ptrs(plan, grads);
   const zk::GroupK g = group_k(plan, group);
   const int64_t P = plan->groups[group].psi_pad;
   // 1. reduce-scatter window by window, each writing its slice of partials
+  //    with the grid fixed above
   cudaError_t e = cudaSuccess;
   int64_t off = 0;
   for (int64_t a = 0; a < P && e == cudaSuccess; a += bucket) {
     const int64_t b = P - a < bucket ? P : a + bucket;
+    const int64_t grid = b == P ? grids.last : grids.full;
     e = zk::launch_reduce_scatter(src, gdtype, g, reduced, a, b, hp->grad_scale, partials + off,
-                                  zk::RS_STORE, st);
-    off += zk::rs_partials_for(plan->n_ranks, gdtype, b - a);
+                                  zk::RS_STORE, st, grid);
+    off += grid;
   }
   // 2. global norm and clip coefficient on the device
   if (e == cudaSuccess) e = zk::launch_norm(partials, off, max_norm, d_norm, d_coef, st);
