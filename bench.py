@@ -641,7 +641,9 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
                           0, 0, g["flat_off"], w.master_sigma, g["flat_off"] + g["psi"])
     m, v = torch.zeros_like(master), torch.zeros_like(master)
     shards = [torch.zeros(ST, dtype=torch.bfloat16, device=dev) for _ in range(N)]
-    slot = [torch.empty(gmax, dtype=torch.bfloat16, device=dev) for _ in range(N)]
+    gdt = torch.bfloat16 if w.grad_dtype == "bf16" else torch.float32
+    zg = Z.ZERO_BF16 if w.grad_dtype == "bf16" else Z.ZERO_F32
+    slot = [torch.empty(gmax, dtype=gdt, device=dev) for _ in range(N)]
     gb = groups[big]
     for r in range(N):
         synth.fill_tensor(slot[r], w.seed, synth.GRAD, 1, r, gb["flat_off"], w.grad_sigma,
@@ -657,8 +659,7 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
         for j, gi in enumerate(rs_order):
             if events is not None:
                 events[j].record(stream)
-            Z.zero_step_group(plan, gi, grads[gi], Z.ZERO_BF16, master, m, v, hp, None, out,
-                              stream)
+            Z.zero_step_group(plan, gi, grads[gi], zg, master, m, v, hp, None, out, stream)
         if events is not None:
             events[G].record(stream)
 
@@ -685,7 +686,7 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
     block_ms = statistics.fmean(x[j] for x in per_launch for j in block)
     res = dict(local_ms=local_ms, launch_sum_ms=launch_sum_ms, block_ms=block_ms,
                block_psi_pad=groups[1]["psi_pad"], P=P, N=N, groups=G, clocks=clocks.summary(),
-               launches_per_step=G)
+               launches_per_step=G, gbytes=2 if w.grad_dtype == "bf16" else 4)
     if kernel_only:
         return res
 
@@ -705,7 +706,7 @@ def bench_stage3(w, steps: int, warmup: int, dist: Dist, use_graph: bool = False
     del a, b
 
     res.update(_stage3_gathers(Z, plan, groups, shards, dev, sa, steps, use_graph))
-    res.update(_stage3_e2e(Z, plan, groups, N, ST, slot, master, m, v, sa, t))
+    res.update(_stage3_e2e(Z, plan, groups, N, ST, slot, zg, master, m, v, sa, t))
     return res
 
 
@@ -766,7 +767,7 @@ def _stage3_gathers(Z, plan, groups, shards, dev, sa, steps, use_graph) -> dict:
     return out
 
 
-def _stage3_e2e(Z, plan, groups, N, ST, slot, master, m, v, sa, t) -> dict:
+def _stage3_e2e(Z, plan, groups, N, ST, slot, zg, master, m, v, sa, t) -> dict:
     """The step end to end through the public API from host memory: the N
     gradient buffers of each group in one page-locked host slot (N x largest
     group, reused for every group, as the device slot is) and the owners'
@@ -775,10 +776,10 @@ def _stage3_e2e(Z, plan, groups, N, ST, slot, master, m, v, sa, t) -> dict:
     link itself; otherwise explicit copies surround each group's step."""
     import torch
     G = len(groups)
-    gmax = slot[0].numel()
-    h2d = N * sum(g["psi_pad"] for g in groups) * 2
+    gmax, gb = slot[0].numel(), slot[0].element_size()
+    h2d = N * sum(g["psi_pad"] for g in groups) * gb
     d2h = N * ST * 2
-    host_bytes = N * gmax * 2 + N * ST * 2
+    host_bytes = N * gmax * gb + N * ST * 2
     ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
     base = dict(e2e_ms=None, h2d=h2d, d2h=d2h, e2e_steps=0)
     if host_bytes * local_ranks() > 0.4 * ram:
@@ -786,8 +787,8 @@ def _stage3_e2e(Z, plan, groups, N, ST, slot, master, m, v, sa, t) -> dict:
                                        f"x {local_ranks()} local ranks exceeds 40% of the "
                                        f"host's {ram / 1e9:.0f} GB")
     pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
-    h_slot = [pinned[r * gmax * 2:(r + 1) * gmax * 2].view(torch.bfloat16) for r in range(N)]
-    off = N * gmax * 2
+    h_slot = [pinned[r * gmax * gb:(r + 1) * gmax * gb].view(slot[0].dtype) for r in range(N)]
+    off = N * gmax * gb
     h_shards = [pinned[off + r * ST * 2:off + (r + 1) * ST * 2].view(torch.bfloat16)
                 for r in range(N)]
     for r in range(N):
@@ -803,12 +804,12 @@ def _stage3_e2e(Z, plan, groups, N, ST, slot, master, m, v, sa, t) -> dict:
         hp = Z.adam_hp(t[0], 1.0 / N)
         for gi in reversed(range(G)):
             if mapped:
-                Z.zero_step_group(plan, gi, h_views[gi], Z.ZERO_BF16, master, m, v, hp, None,
+                Z.zero_step_group(plan, gi, h_views[gi], zg, master, m, v, hp, None,
                                   h_shards, sa)
             else:
                 for r in range(N):
                     d_views[gi][r].copy_(h_views[gi][r], non_blocking=True)
-                Z.zero_step_group(plan, gi, d_views[gi], Z.ZERO_BF16, master, m, v, hp, None,
+                Z.zero_step_group(plan, gi, d_views[gi], zg, master, m, v, hp, None,
                                   dshards, sa)
         if not mapped:
             for r in range(N):
@@ -1059,7 +1060,8 @@ def workload_config(w, n_gpus: int) -> dict:
     return {"workload": f"{w.name}: one stage-3 step = per layer group (34, reverse order) "
                         "fused reduce-scatter + scale + Adam writing each owner's bf16 shard",
             **common, "groups": len(set(w.groups)), "gathered": "bf16 owner shards",
-            "grads": "each group's N buffers are prefixes of one resident N x 202M bf16 slot",
+            "grads": f"each group's N buffers are prefixes of one resident N x 202M "
+                     f"{w.grad_dtype} slot",
             "bytes_per_step": abytes,
             "l2": f"inputs {abytes / 1e9:.0f} GB per step > L2 129 MB, no flush"}
 
@@ -1167,12 +1169,12 @@ def stage3_line(w, args, dist) -> dict:
     ms = dist.max(r["local_ms"])
     n_gpus = dist.world
     pk = _peaks()
-    step_bytes = algorithmic_bytes(N, P, 2)
-    block_bytes = algorithmic_bytes(N, r["block_psi_pad"], 2)
+    step_bytes = algorithmic_bytes(N, P, r["gbytes"])
+    block_bytes = algorithmic_bytes(N, r["block_psi_pad"], r["gbytes"])
     achieved = block_bytes / (r["block_ms"] * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "unit": "GB/s", "frac": achieved / pk["peak"],
-            **pk, "kernel": "fused_kernel<16,bf16> (zero_step_group), one transformer block's "
-                            "group per launch",
+            **pk, "kernel": f"fused_kernel<{N},{w.grad_dtype}> (zero_step_group), one "
+                            "transformer block's group per launch",
             "algorithmic_bytes_per_launch": block_bytes,
             "traffic": profiled_traffic("fused_kernel", w.name, "fused_kernel_block"),
             "step_launches_gbs": step_bytes / (r["launch_sum_ms"] * 1e-3) / 1e9}

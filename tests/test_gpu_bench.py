@@ -25,10 +25,12 @@ def _line(*args):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("workload", ["llama-7b-stage3", "gpt2-small", "llama-1.4b"])
-def test_bench_line_keys(cuda, workload):
+@pytest.mark.parametrize("workload,extra", [("llama-7b-stage3", ()), ("gpt2-small", ()),
+                                            ("llama-1.4b", ()),
+                                            ("llama-7b-stage3", ("--grad-dtype", "f32"))])
+def test_bench_line_keys(cuda, workload, extra):
     d = _line("--workload", workload, "--scale", "16", "--steps", "3", "--warmup", "3",
-              "--no-cpu-baseline")
+              "--no-cpu-baseline", *extra)
     for k in KEYS:
         assert k in d, k
     assert d["n_gpus"] == 1 and d["steps"] == 3 and d["higher_is_better"] is True
@@ -43,6 +45,9 @@ def test_bench_line_keys(cuda, workload):
         assert k in e, k
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0 and e["value"] > 0
     assert d["gpu_launches"] > 0 and "workload" in d["config"]
+    if extra:
+        assert d["config"]["grad_dtype"] == "f32" and "f32" in r["kernel"]
+        assert d["config"]["bytes_per_step"] == d["config"]["psi"] * (16 * 4 + 26)
     if workload == "llama-7b-stage3":
         assert d["gpu_launches"] == 34 * 3 and d["config"]["groups"] == 34
         g = d["gather"]
