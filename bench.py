@@ -601,6 +601,9 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = F
 # Rounds of the arithmetic-bound stand-in consumer (zero_layer_checksum): at 64
 # its 68 launches over the Llama-7B groups take about 3.5x the gathers.
 ARITH_ROUNDS = 64
+# Tokens of the tensor-core consumer's activation batch: at 2048 its 68 bf16
+# GEMMs over the Llama-7B layers (1.8 PFLOP/s) take about 4x the gathers.
+GEMM_TOKENS = 2048
 
 
 def _hidden(gathers_ms: float, consumers_ms: float, schedule_ms: float) -> float:
@@ -758,12 +761,58 @@ def _stage3_gathers(Z, plan, groups, shards, dev, sa, steps, use_graph) -> dict:
         sa.wait_stream(gs)
         torch.cuda.synchronize()
         runs["schedule_graph_ms"] = graph.replay
+    # a tensor-core consumer: each gathered layer used as a [d, cols] bf16
+    # weight matrix (cols = psi_pad/d rounded down to a multiple of 64, so its
+    # rows stay 16-byte aligned and cuBLAS runs at full speed) against
+    # GEMM_TOKENS activations (a cuBLAS GEMM through torch.matmul) -- the
+    # matrix products prefetching is meant to hide -- in the same two-stream
+    # schedule as zero_stage3_gather_pass
+    d = 4096 if min(g["psi_pad"] for g in groups) >= 4096 * 256 else 256
+    x = torch.randn(GEMM_TOKENS, d, device=dev).to(torch.bfloat16)
+    y = torch.empty(GEMM_TOKENS * (gmax // d), dtype=torch.bfloat16, device=dev)
+    cols = [groups[gi]["psi_pad"] // d // 64 * 64 for gi in order]    # 16-byte aligned rows
+    ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+
+    def gemm(j):
+        w = bufs[j % 2][:d * cols[j]].view(d, cols[j])
+        torch.matmul(x, w, out=y[:GEMM_TOKENS * cols[j]].view(GEMM_TOKENS, cols[j]))
+
+    def gemms():
+        with torch.cuda.stream(sa):
+            for j in range(len(order)):
+                gemm(j)
+
+    def gemm_schedule():
+        start = torch.cuda.Event()
+        start.record(sa)
+        sb.wait_event(start)
+
+        def issue(j):
+            if j >= 2:
+                sb.wait_event(done[j % 2])
+            Z.zero_gather_layer(plan, order[j], shards, Z.ZERO_BF16, bufs[j % 2], sb)
+            ready[j % 2].record(sb)
+
+        issue(0)
+        with torch.cuda.stream(sa):
+            for j in range(len(order)):
+                if j + 1 < len(order):
+                    issue(j + 1)
+                sa.wait_event(ready[j % 2])
+                gemm(j)
+                done[j % 2].record(sa)
+
+    runs["gemm_consumers_only_ms"] = gemms
+    runs["gemm_schedule_ms"] = gemm_schedule
     for f in runs.values():           # warm-up
         timed(f)
     out = {k: statistics.fmean(timed(f) for _ in range(max(1, min(steps, 10))))
            for k, f in runs.items()}
     out["gather_elems"] = 2 * sum(g["psi_pad"] for g in groups)
     out["gather_launches"] = len(order)
+    out["gemm_flops"] = 2 * GEMM_TOKENS * d * sum(cols)
+    out["gemm_shape"] = f"[{GEMM_TOKENS}, {d}] x [{d}, psi_pad/{d} to a multiple of 64] per layer"
     return out
 
 
@@ -1066,6 +1115,15 @@ def workload_config(w, n_gpus: int) -> dict:
             "l2": f"inputs {abytes / 1e9:.0f} GB per step > L2 129 MB, no flush"}
 
 
+def _bf16_peak():
+    """Measured dense bf16 TFLOP/s (burst) of this machine's GPUs, or None."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def _peaks() -> dict:
     peak, kind = measured_hbm_peak()
     return {"peak": peak, "peak_kind": kind, "peak_nominal_gbs": NOMINAL_HBM_GBS}
@@ -1203,6 +1261,15 @@ def stage3_line(w, args, dist) -> dict:
                                     r["schedule_arith_ms"])}}
     if "schedule_graph_ms" in r:
         gather["schedule_graph_ms"] = r["schedule_graph_ms"]
+    tf_peak = _bf16_peak()
+    gather["gemm_consumer"] = {
+        "shape": r["gemm_shape"], "consumers_only_ms": r["gemm_consumers_only_ms"],
+        "consumer_tflops": r["gemm_flops"] / (r["gemm_consumers_only_ms"] * 1e-3) / 1e12,
+        "consumer_frac_of_bf16_peak": (r["gemm_flops"] / (r["gemm_consumers_only_ms"] * 1e-3)
+                                       / 1e12 / tf_peak) if tf_peak else None,
+        "schedule_ms": r["gemm_schedule_ms"],
+        "hidden": _hidden(r["gathers_only_ms"], r["gemm_consumers_only_ms"],
+                          r["gemm_schedule_ms"])}
     e2e_ms = dist.max(r["e2e_ms"]) if r["e2e_ms"] is not None else None
     return {"metric": METRIC, "value": n_gpus * w.psi / (ms * 1e-3) / 1e9,
             "unit": "Gparams/s", "n_gpus": n_gpus, "steps": args.steps, "warmup": args.warmup,
