@@ -412,7 +412,12 @@ def bench_fused(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = Fals
                     e2e_transfer=f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
                                  f"x {local_ranks()} local ranks exceeds 40% of the host's "
                                  f"{ram / 1e9:.0f} GB")
-    pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
+    try:
+        pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
+    except RuntimeError as err:       # the host could not pin that much: no e2e leg
+        return dict(local_ms=local_ms, launch_ms=launch_ms, e2e_ms=None, psi=w.psi, psi_pad=P,
+                    n_ranks=N, gbytes=gbytes, copy_gbs=copy_gbs, clocks=clocks.summary(),
+                    h2d=N * P * gbytes, d2h=P * 2, e2e_steps=0, e2e_transfer=f"skipped: {err}")
     h_grads = [pinned[r * P * gbytes:(r + 1) * P * gbytes].view(gdt) for r in range(N)]
     for r in range(N):
         h_grads[r].copy_(grads[r])
@@ -562,7 +567,11 @@ def bench_bucketed(w, steps: int, warmup: int, dist: Dist, kernel_only: bool = F
                                f"x {local_ranks()} local ranks exceeds 40% of the host's "
                                f"{ram / 1e9:.0f} GB")
         return res
-    pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
+    try:
+        pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
+    except RuntimeError as err:       # the host could not pin that much: no e2e leg
+        res["e2e_transfer"] = f"skipped: {err}"
+        return res
     h_grads = [pinned[r * P * gb:(r + 1) * P * gb].view(gdt) for r in range(N)]
     h_out = pinned[N * P * gb:].view(torch.bfloat16)
     for r in range(N):
@@ -835,7 +844,10 @@ def _stage3_e2e(Z, plan, groups, N, ST, slot, zg, master, m, v, sa, t) -> dict:
         return dict(base, e2e_transfer=f"skipped: {host_bytes / 1e9:.0f} GB of pinned host memory "
                                        f"x {local_ranks()} local ranks exceeds 40% of the "
                                        f"host's {ram / 1e9:.0f} GB")
-    pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
+    try:
+        pinned, free_pinned, numa = pinned_host_buffer(host_bytes, near_gpu=True)
+    except RuntimeError as err:       # the host could not pin that much: no e2e leg
+        return dict(base, e2e_transfer=f"skipped: {err}")
     h_slot = [pinned[r * gmax * gb:(r + 1) * gmax * gb].view(slot[0].dtype) for r in range(N)]
     off = N * gmax * gb
     h_shards = [pinned[off + r * ST * 2:off + (r + 1) * ST * 2].view(torch.bfloat16)
