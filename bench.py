@@ -1328,15 +1328,17 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="llama-7b-stage3 (default), gpt2-small, gpt2-medium, llama-1.4b or tiny")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale", type=int, default=1,
                     help="shrink the workload's tensors by this factor (profiling cases)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the step kernels: no copy peak, gathers, e2e or CPU baseline")
     ap.add_argument("--graph", action="store_true",
-                    help="replay one CUDA-graph-captured step (device-resident Adam step state); "
-                         "stage-3 workload: also time the gather pass replayed from a graph")
+                    help="fused workloads: time CUDA-graph replays of the step (device-resident "
+                         "Adam step state); stage-3 workload: also time the gather pass "
+                         "replayed from a graph")
     ap.add_argument("--graph-steps", type=int, default=1,
                     help="with --graph: steps captured in one graph (amortises the replay launch)")
     ap.add_argument("--grad-dtype", choices=["bf16", "f32"], default=None,
